@@ -1,0 +1,208 @@
+/*
+ * disco.h -- C ABI of the GB300 (sm_103a) DISCO convolution library.
+ *
+ * DISCO = discrete-continuous convolution on the sphere.  The operations
+ * follow the DISCO Kernel Development Guide (torch-harmonics), whose
+ * §Architecture snapshot lists the three kernels this library provides:
+ *   forward   "CSR sparse contraction inp -> (B,C,K,H,W)"
+ *   backward  "CSR transpose contraction (B,C,K,H,W) -> inp"
+ *   fused     "contraction + einsum"  (y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo])
+ * and whose §kpacked layout describes the neighbour-list form of psi built
+ * once at init ("converts CSR psi to kpacked layout at init time").
+ *
+ * Conventions (all entry points):
+ *  - Every tensor argument is a DEVICE pointer to a dense, C-contiguous array
+ *    in the layout stated, 16-byte aligned, owned by the caller.  The library
+ *    never allocates, frees or keeps a reference to caller memory beyond the
+ *    call, and never synchronises the stream except where stated.
+ *  - Outputs are fully overwritten (never accumulated into).
+ *  - All validation happens on the host before any launch; a failed check
+ *    returns a negative disco_status and launches nothing.  disco_last_error()
+ *    then returns a message for the calling thread.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous unless stated.
+ *  - Accumulation is fp32; the output dtype equals the input dtype.
+ *  - The device must have compute capability 10.3 (sm_103a);
+ *    DISCO_ERR_UNSUPPORTED_DEVICE otherwise.
+ */
+#ifndef DISCO_GB300_H
+#define DISCO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DISCO_API __attribute__((visibility("default")))
+#else
+#define DISCO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DISCO_OK = 0,
+  DISCO_ERR_INVALID_ARG = -1,        /* null pointer, bad size, inconsistent psi */
+  DISCO_ERR_UNSUPPORTED = -2,        /* valid but not supported (W_in % W_out, K, dtype, s) */
+  DISCO_ERR_ALIGNMENT = -3,          /* a pointer is not 16-byte aligned */
+  DISCO_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
+  DISCO_ERR_LAUNCH = -5,             /* a kernel launch was rejected by the runtime */
+  DISCO_ERR_CUDA = -6,               /* another CUDA runtime call failed */
+  DISCO_ERR_WORKSPACE = -7           /* workspace missing or too small */
+} disco_status;
+
+typedef enum { DISCO_F32 = 0, DISCO_BF16 = 1 } disco_dtype;
+
+/* Equiangular grid.  poles = 0: colatitude (i + 1/2) pi / nlat;
+   poles = 1: colatitude i pi / (nlat - 1) (both poles on the grid).
+   Longitude 2 pi j / nlon in both cases. */
+typedef struct {
+  int32_t nlat, nlon, poles;
+} disco_grid;
+
+/* Filter basis on geodesic distance d.  n_radial hats of width
+   cutoff / n_radial centred at r * width (hat_r(d) = max(0, 1 - |d - r w| / w)).
+   kind 0 (isotropic): K = n_radial, basis k = hat_k.
+   kind 1 (anisotropic): K = 3 n_radial, basis k = 3 r + a is hat_r times
+   {1, cos(beta), sin(beta)}[a], beta the bearing from the output point to the
+   input point (0 = north, pi/2 = east).
+   Values are hat * angular factor * sin(colatitude_in) / N(r, ho) with N the
+   sum of hat_r * sin(colatitude_in) over ring r's support (support: hat > 1e-9
+   and sin(colatitude_in) > 0; pole rows of a pole grid carry weight 0). */
+typedef struct {
+  int32_t kind;
+  int32_t n_radial;
+  double cutoff; /* radians */
+} disco_basis;
+
+/* One (ho, hi) segment of psi: the input row hi seen from output row ho is one
+   contiguous wrapped window of columns, symmetric about offset 0.  Offsets
+   delta in [0, D] address the mirrored pairs (delta, -delta); the weights of
+   the self-mirrored offsets (0 and, on a full ring of even width, W_in/2) are
+   stored halved so every step is a pair. */
+typedef struct {
+  int32_t ho, hi;
+  int32_t D;     /* pair steps are delta = 0 .. D */
+  int32_t hoff;  /* row of this run's first pair weight in psi.hval */
+  int32_t e0;    /* first entry of the run in the union (kpacked) arrays */
+  int32_t len;   /* entries of the run in the union arrays (2m+1, or W_in) */
+  int32_t npair; /* mirrored pairs delta = 1 .. npair */
+  int32_t anti;  /* 1 if the run holds the unpaired antipodal column */
+} disco_run;
+
+/* psi: sizes set by disco_psi_plan, device pointers (into the caller's psi
+   buffer) set by disco_build_psi_kpacked.  Read-only after the build.
+   Index structures are int32; values fp32. */
+typedef struct {
+  disco_grid grid_in, grid_out;
+  disco_basis basis;
+  int32_t K;        /* basis functions */
+  int32_t K_pad;    /* K rounded up to a multiple of 8 (page: K_PAD = ceil(K/8)*8) */
+  int32_t s;        /* W_in / W_out */
+  int32_t max_row;  /* largest union row (neighbours of one output row) */
+  int64_t nnz;      /* union neighbours summed over output rows */
+  int64_t nnz_csr;  /* CSR non-zeros summed over (k, ho) rows */
+  int64_t nruns;    /* (ho, hi) segments */
+  int64_t nhval;    /* rows of hval */
+  size_t bytes;     /* device bytes disco_build_psi_kpacked needs */
+  /* Union ("kpacked") layout, shared across k (§kpacked layout):
+     neighbours of output row ho (for output longitude 0) are entries
+     row_ptr[ho] .. row_ptr[ho+1]-1, ordered by hi ascending then by the
+     signed column offset ((wi + floor(W/2)) mod W) - floor(W/2) ascending. */
+  int32_t* row_ptr;     /* [Hout + 1] */
+  int32_t* idx;         /* [nnz][2] = (hi, wi) */
+  float* val;           /* [nnz][K_pad], zero for k >= K and non-structural k */
+  /* CSR layout (§Architecture snapshot): row k * Hout + ho, column hi * W_in + wi,
+     same neighbour order, only entries whose ring is structural. */
+  int32_t* csr_row_ptr; /* [K * Hout + 1] */
+  int32_t* csr_col;     /* [nnz_csr] */
+  float* csr_val;       /* [nnz_csr] */
+  /* Kernel-side forms derived from the above. */
+  int32_t* run_ptr;     /* [Hout + 1]: runs of output row ho */
+  disco_run* runs;      /* [nruns], ordered by (ho, hi) */
+  int32_t* trun_ptr;    /* [Hin + 1]: runs that read input row hi */
+  int32_t* truns;       /* [nruns]: run indices ordered by (hi, ho) */
+  float* hval;          /* [nhval][K_pad]: pair weights, see disco_run */
+  int32_t* row_order;   /* [Hout]: output rows by descending work (launch order) */
+} disco_psi;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+DISCO_API int32_t disco_version(void);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+DISCO_API const char* disco_last_error(void);
+
+/* Host only, no device work.  Bytes of device workspace that disco_psi_plan
+   and disco_build_psi_kpacked need for these grids and basis. */
+DISCO_API int disco_psi_workspace_bytes(const disco_grid* grid_in, const disco_grid* grid_out,
+                              const disco_basis* basis, size_t* bytes);
+
+/* Init time; BLOCKS the host (one device-to-host copy of per-row counts).
+   Runs the support-counting kernels (fp64 geometry) on `stream` into
+   `workspace` and fills the sizes of *psi (pointers are cleared).  The
+   workspace contents are consumed by disco_build_psi_kpacked and must be left
+   untouched in between.  Requires W_in % W_out == 0, 1 <= K <= 16, nlat >= 2
+   (>= 3 on a pole grid), nlon >= 1. */
+DISCO_API int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_out,
+                   const disco_basis* basis, void* workspace, size_t workspace_bytes,
+                   void* stream, disco_psi* psi);
+
+/* Init time, asynchronous.  Builds psi (§kpacked layout, CSR layout and the
+   kernel-side forms) into `buffer` (device, >= psi->bytes bytes, 256-byte
+   aligned) and sets the pointers of *psi into it.  Values are computed in fp64
+   on the device and stored as fp32. */
+DISCO_API int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Forward S2 contraction (§Architecture snapshot "forward"; §Backward
+   direction: gather, each output pixel reads a bounded neighbourhood):
+     X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]
+                        * x[b,c,hi,(wi + wo*s) mod W_in]
+   x: [B, C, H_in, W_in], X: [B, C, K, H_out, W_out], both `dtype`.
+   Supports s in {1, 2}; W_out % 8 == 0 for bf16 and % 4 == 0 for fp32. */
+DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
+              disco_dtype dtype, void* stream);
+
+/* Transpose contraction (§Architecture snapshot "backward"; §Backward
+   direction: gather direction, each input pixel accumulates from its
+   neighbourhood, no atomics):  gx = psi^T G, i.e.
+     gx[b,c,hi,wi] = sum_{k,ho,wo} sum_{wi0: (wi0 + wo*s) mod W_in = wi}
+                       psi[k,ho,hi,wi0] * G[b,c,k,ho,wo]
+   G: [B, C, K, H_out, W_out], gx: [B, C, H_in, W_in], both `dtype`.
+   Each thread block owns whole input rows (latitude-row ownership). */
+DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
+              disco_dtype dtype, void* stream);
+
+/* Fused convolution (§Architecture snapshot "_disco_s2_fused_conv_optimized:
+   contraction + einsum"):  y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo]
+   with X the forward contraction, which never leaves the chip: it is built
+   in shared memory as bf16 and contracted on the tcgen05 tensor cores with
+   fp32 accumulation in tensor memory.
+   x: [B, Cin, H_in, W_in] bf16, W: [Cout, Cin, K] bf16, y: [B, Cout, H_out, W_out] bf16.
+   dtype must be DISCO_BF16; Cin % 16 == 0; Cout <= 256. */
+DISCO_API int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
+                     int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
+                     void* stream);
+
+/* Device workspace bytes of disco_fused_conv_bwd_input (the bf16 intermediate
+   dX[B, Cin, K, H_out, W_out]). */
+DISCO_API size_t disco_fused_conv_bwd_input_workspace_bytes(const disco_psi* psi, int32_t B,
+                                                  int32_t Cin, disco_dtype dtype);
+
+/* Input gradient of the fused convolution:
+     dX[b,c,k,ho,wo] = sum_o W[o,c,k] dy[b,o,ho,wo]   (tcgen05 tensor cores)
+     gx = psi^T dX                                    (the transpose contraction)
+   dy: [B, Cout, H_out, W_out] bf16, W: [Cout, Cin, K] bf16, gx: [B, Cin, H_in, W_in] bf16.
+   dX is kept in `workspace` (>= disco_fused_conv_bwd_input_workspace_bytes)
+   as bf16.  dtype must be DISCO_BF16; Cout % 16 == 0. */
+DISCO_API int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, const void* W,
+                               void* gx, int32_t B, int32_t Cin, int32_t Cout,
+                               disco_dtype dtype, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DISCO_GB300_H */

@@ -1,0 +1,251 @@
+"""GB300 (sm_103a) DISCO convolution on the sphere: Python binding of the C ABI.
+
+The binding only marshals arguments: every step runs in the CUDA library
+``_build/libdisco_gb300_<arch>.so`` (built by ``build.py``).  If the library
+is missing, importing the functions raises; there is no fallback.
+
+The functions carry the names of the C ABI (``include/disco.h``) and take
+torch tensors for device memory; torch's current CUDA stream is used unless a
+stream is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build_mod
+
+__all__ = [
+    "DiscoError", "disco_grid", "disco_basis", "disco_run", "disco_psi", "Psi",
+    "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
+    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
+    "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
+    "library_path", "load_library", "EXPORTED_SYMBOLS",
+]
+
+DISCO_F32, DISCO_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = [
+    "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
+    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
+    "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
+]
+
+
+class DiscoError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"disco status {status}: {message}")
+        self.status = status
+
+
+class disco_grid(ctypes.Structure):
+    _fields_ = [("nlat", ctypes.c_int32), ("nlon", ctypes.c_int32), ("poles", ctypes.c_int32)]
+
+
+class disco_basis(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("n_radial", ctypes.c_int32), ("cutoff", ctypes.c_double)]
+
+
+class disco_run(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("ho", "hi", "D", "hoff", "e0", "len", "npair", "anti")]
+
+
+_PSI_ARRAYS = ["row_ptr", "idx", "val", "csr_row_ptr", "csr_col", "csr_val", "run_ptr", "runs",
+               "trun_ptr", "truns", "hval", "row_order"]
+
+
+class disco_psi(ctypes.Structure):
+    _fields_ = [("grid_in", disco_grid), ("grid_out", disco_grid), ("basis", disco_basis),
+                ("K", ctypes.c_int32), ("K_pad", ctypes.c_int32), ("s", ctypes.c_int32),
+                ("max_row", ctypes.c_int32), ("nnz", ctypes.c_int64), ("nnz_csr", ctypes.c_int64),
+                ("nruns", ctypes.c_int64), ("nhval", ctypes.c_int64), ("bytes", ctypes.c_size_t)] + \
+               [(n, ctypes.c_void_p) for n in _PSI_ARRAYS]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build_mod.LIB
+
+
+def load_library():
+    """Loads the built library; raises if it is missing (no fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"DISCO CUDA library not built: {path} is missing "
+                           "(run `python -m sparse_spherical_convolution_gb300.build`)")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    PG, PB, PP = ctypes.POINTER(disco_grid), ctypes.POINTER(disco_basis), ctypes.POINTER(disco_psi)
+    lib.disco_version.restype = I32
+    lib.disco_version.argtypes = []
+    lib.disco_last_error.restype = ctypes.c_char_p
+    lib.disco_last_error.argtypes = []
+    lib.disco_psi_workspace_bytes.restype = ctypes.c_int
+    lib.disco_psi_workspace_bytes.argtypes = [PG, PG, PB, ctypes.POINTER(SZ)]
+    lib.disco_psi_plan.restype = ctypes.c_int
+    lib.disco_psi_plan.argtypes = [PG, PG, PB, P, SZ, P, PP]
+    lib.disco_build_psi_kpacked.restype = ctypes.c_int
+    lib.disco_build_psi_kpacked.argtypes = [PP, P, SZ, P, SZ, P]
+    lib.disco_fwd.restype = ctypes.c_int
+    lib.disco_fwd.argtypes = [PP, P, P, I32, I32, ctypes.c_int, P]
+    lib.disco_bwd.restype = ctypes.c_int
+    lib.disco_bwd.argtypes = [PP, P, P, I32, I32, ctypes.c_int, P]
+    lib.disco_fused_conv.restype = ctypes.c_int
+    lib.disco_fused_conv.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P]
+    lib.disco_fused_conv_bwd_input_workspace_bytes.restype = SZ
+    lib.disco_fused_conv_bwd_input_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
+    lib.disco_fused_conv_bwd_input.restype = ctypes.c_int
+    lib.disco_fused_conv_bwd_input.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise DiscoError(status, load_library().disco_last_error().decode())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return DISCO_F32
+    if t.dtype == torch.bfloat16:
+        return DISCO_BF16
+    raise DiscoError(-2, f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise DiscoError(-1, "tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ------------------------------------------------------------------ ABI calls
+
+def disco_version() -> int:
+    return load_library().disco_version()
+
+
+def disco_last_error() -> str:
+    return load_library().disco_last_error().decode()
+
+
+def _grid(g) -> disco_grid:
+    return g if isinstance(g, disco_grid) else disco_grid(*[int(v) for v in g])
+
+
+def _basis(kind, n_radial=None, cutoff=None) -> disco_basis:
+    if isinstance(kind, disco_basis):
+        return kind
+    return disco_basis(int(kind), int(n_radial), float(cutoff))
+
+
+def disco_psi_workspace_bytes(grid_in, grid_out, basis) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().disco_psi_workspace_bytes(
+        ctypes.byref(_grid(grid_in)), ctypes.byref(_grid(grid_out)), ctypes.byref(basis),
+        ctypes.byref(n)))
+    return n.value
+
+
+def disco_psi_plan(grid_in, grid_out, basis, workspace, stream=None) -> disco_psi:
+    psi = disco_psi()
+    _check(load_library().disco_psi_plan(
+        ctypes.byref(_grid(grid_in)), ctypes.byref(_grid(grid_out)), ctypes.byref(basis),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        ctypes.byref(psi)))
+    return psi
+
+
+def disco_build_psi_kpacked(psi: disco_psi, buffer, workspace, stream=None) -> None:
+    _check(load_library().disco_build_psi_kpacked(
+        ctypes.byref(psi), _ptr(buffer), buffer.numel() * buffer.element_size(), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def disco_fwd(psi: disco_psi, x, X, B: int, C: int, stream=None) -> None:
+    _check(load_library().disco_fwd(ctypes.byref(psi), _ptr(x), _ptr(X), B, C, _dtype(x),
+                                    _stream(stream)))
+
+
+def disco_bwd(psi: disco_psi, G, gx, B: int, C: int, stream=None) -> None:
+    _check(load_library().disco_bwd(ctypes.byref(psi), _ptr(G), _ptr(gx), B, C, _dtype(G),
+                                    _stream(stream)))
+
+
+def disco_fused_conv(psi: disco_psi, x, W, y, B: int, Cin: int, Cout: int, stream=None) -> None:
+    _check(load_library().disco_fused_conv(ctypes.byref(psi), _ptr(x), _ptr(W), _ptr(y), B, Cin,
+                                           Cout, _dtype(x), _stream(stream)))
+
+
+def disco_fused_conv_bwd_input_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:
+    return load_library().disco_fused_conv_bwd_input_workspace_bytes(ctypes.byref(psi), B, Cin, dtype)
+
+
+def disco_fused_conv_bwd_input(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout: int,
+                               workspace, stream=None) -> None:
+    _check(load_library().disco_fused_conv_bwd_input(
+        ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy),
+        _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
+        _stream(stream)))
+
+
+# ------------------------------------------------------------ convenience
+
+class Psi:
+    """psi built on the device, with the torch buffers that own its memory.
+
+    ``Psi(grid_in, grid_out, kind, n_radial, cutoff)`` runs disco_psi_plan and
+    disco_build_psi_kpacked on the current CUDA device and stream."""
+
+    _DT = {"row_ptr": "int32", "idx": "int32", "val": "float32", "csr_row_ptr": "int32",
+           "csr_col": "int32", "csr_val": "float32", "run_ptr": "int32", "runs": "int32",
+           "trun_ptr": "int32", "truns": "int32", "hval": "float32", "row_order": "int32"}
+
+    def __init__(self, grid_in, grid_out, kind: int, n_radial: int, cutoff: float, stream=None):
+        import torch
+        self.basis = _basis(kind, n_radial, cutoff)
+        gi, go = _grid(grid_in), _grid(grid_out)
+        wsb = disco_psi_workspace_bytes(gi, go, self.basis)
+        self.workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        self.c = disco_psi_plan(gi, go, self.basis, self.workspace, stream)
+        self.buffer = torch.empty(max(self.c.bytes, 256), dtype=torch.uint8, device="cuda")
+        disco_build_psi_kpacked(self.c, self.buffer, self.workspace, stream)
+
+    def _sizes(self):
+        c = self.c
+        Hin, Hout = c.grid_in.nlat, c.grid_out.nlat
+        return {"row_ptr": (Hout + 1,), "idx": (c.nnz, 2), "val": (c.nnz, c.K_pad),
+                "csr_row_ptr": (c.K * Hout + 1,), "csr_col": (c.nnz_csr,),
+                "csr_val": (c.nnz_csr,), "run_ptr": (Hout + 1,), "runs": (c.nruns, 8),
+                "trun_ptr": (Hin + 1,), "truns": (c.nruns,), "hval": (c.nhval, c.K_pad),
+                "row_order": (Hout,)}
+
+    def tensor(self, name: str):
+        """Device view of one psi array (for inspection and tests)."""
+        import torch
+        ptr = getattr(self.c, name)
+        off = ptr - self.buffer.data_ptr()
+        shape = self._sizes()[name]
+        n = 1
+        for v in shape:
+            n *= int(v)
+        dt = getattr(torch, self._DT[name])
+        esz = torch.tensor([], dtype=dt).element_size()
+        return self.buffer[off:off + n * esz].view(dt).view(*[int(v) for v in shape])

@@ -1,0 +1,39 @@
+// disco_internal.cuh -- helpers shared by the library's translation units
+// (error reporting, device checks, bf16 conversion).  Not part of the ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "disco.h"
+
+namespace disco {
+
+// Records `msg` (printf-style) as this thread's last error and returns `st`.
+int fail(int st, const char* fmt, ...);
+
+// 0 if the current device is compute capability 10.3, else a failure status.
+int check_device();
+
+// Launch-error check right after a launch.
+int check_launch(const char* what);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the pieces of psi every hot call relies on.
+int check_psi(const disco_psi* psi);
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+}  // namespace disco

@@ -1,0 +1,570 @@
+// disco_psi.cu -- device construction of the DISCO filter tensor psi.
+//
+// DISCO Kernel Development Guide (torch-harmonics), §kpacked layout: psi is
+// converted once at init into a neighbour list shared across the K basis
+// functions, with the values of all k side by side (K padded to K_PAD =
+// ceil(K/8)*8).  Here the whole build runs on the GPU in fp64:
+//
+//   count   (one block per output row)  for each input row hi, the half-width
+//           m of the union support (the support of one input row is a
+//           contiguous window symmetric about offset 0, because the distance
+//           grows with |longitude offset|), per-ring structural counts and
+//           per-ring sums of hat * quadrature;
+//   plan    per-row totals are copied to the host to size the buffers;
+//   scan    row pointers, CSR row pointers, run and pair-weight offsets;
+//   fill    indices, fp32 values (union layout, CSR layout, pair weights),
+//           run table;
+//   trans   the transposed run list (runs grouped by input row) for the
+//           gather-direction transpose contraction.
+//
+// Definitions (the page names the operations but not the basis, so these are
+// the plainest readings of the workload text):
+//   colatitude  (i + 1/2) pi / H, or i pi / (H - 1) on a pole grid (pi exactly at i = H-1)
+//   distance    haversine great-circle distance, longitude offset 2 pi delta / W_in
+//   hats        width w = cutoff / R, h_r(d) = max(0, 1 - |d - r w| / w)
+//   bearing     atan2(sin dphi sin th_i, sin th_o cos th_i - cos th_o sin th_i cos dphi)
+//   quadrature  sin(colatitude), exactly 0 on the pole rows of a pole grid
+//   support     h_r > 1e-9 and quadrature > 0
+//   value       h_r * {1, cos beta, sin beta}[a] * q / N(r, ho), N = sum of h_r q over ring r
+// All fp64 arithmetic uses explicitly rounded operations (no fused
+// multiply-add), so the index structures are bit-exact and the values agree
+// with a plain fp64 evaluation to the last fp32 bit in all but rare ties.
+
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "disco_internal.cuh"
+
+namespace disco {
+namespace {
+
+constexpr double kPi = 3.14159265358979323846;
+constexpr double kTauSupport = 1e-9;
+constexpr double kCoincident = 1e-12;
+constexpr int kMaxRad = 8;
+
+struct PsiGeom {
+  int Hin, Win, pin, Hout, Wout, pout;
+  int kind, R, K, Kp;
+  double cutoff, width;
+};
+
+__device__ double colat(int H, int poles, int i) {
+  if (poles) {
+    if (i == H - 1) return kPi;
+    return __ddiv_rn(__dmul_rn((double)i, kPi), (double)(H - 1));
+  }
+  return __ddiv_rn(__dmul_rn(__dadd_rn((double)i, 0.5), kPi), (double)H);
+}
+
+__device__ double quadw(int H, int poles, int i) {
+  if (poles && (i == 0 || i == H - 1)) return 0.0;
+  return sin(colat(H, poles, i));
+}
+
+// distance and bearing from (th_o, 0) to (th_i, 2 pi delta / W)
+__device__ void geometry(double th_o, double th_i, int delta, int W, double* d, double* beta) {
+  int ad = delta < 0 ? -delta : delta;
+  double half = __ddiv_rn(__dmul_rn(kPi, (double)ad), (double)W);
+  double s1 = sin(__dmul_rn(0.5, __dsub_rn(th_i, th_o)));
+  double s2 = sin(half);
+  double so = sin(th_o), si = sin(th_i), co = cos(th_o), ci = cos(th_i);
+  double hav = __dadd_rn(__dmul_rn(s1, s1), __dmul_rn(__dmul_rn(so, si), __dmul_rn(s2, s2)));
+  if (hav > 1.0) hav = 1.0;
+  *d = __dmul_rn(2.0, asin(sqrt(hav)));
+  double twice = __dmul_rn(2.0, half);
+  double sdp = sin(twice), cdp = cos(twice);
+  if (delta < 0) sdp = -sdp;
+  *beta = atan2(__dmul_rn(sdp, si), __dsub_rn(__dmul_rn(so, ci), __dmul_rn(__dmul_rn(co, si), cdp)));
+}
+
+__device__ double hat(double d, int r, double width) {
+  double v = __dsub_rn(1.0, __ddiv_rn(fabs(__dsub_rn(d, __dmul_rn((double)r, width))), width));
+  return v > 0.0 ? v : 0.0;
+}
+
+// largest |delta| of one ring (W/2 for even W: the antipodal column)
+__device__ __host__ inline int half_ring(int W) { return W / 2; }
+
+// union support at |delta| = ad; fills hats and structural flags
+__device__ bool support_at(const PsiGeom& g, double th_o, double th_i, double q, int ad,
+                           double* h, bool* st, double* d, double* beta) {
+  geometry(th_o, th_i, ad, g.Win, d, beta);
+  bool any = false;
+  for (int r = 0; r < g.R; ++r) {
+    h[r] = hat(*d, r, g.width);
+    st[r] = (h[r] > kTauSupport) && (q > 0.0);
+    any |= st[r];
+  }
+  return any;
+}
+
+// entries of a run with |delta| = ad: 1 for offset 0 and for the antipodal
+// column of an even ring, else 2 (delta and -delta)
+__device__ __host__ inline int mult_at(int ad, int W) {
+  return (ad == 0 || (2 * ad == W)) ? 1 : 2;
+}
+
+__device__ __host__ inline int run_len(int m, int W) {
+  if (m < 0) return 0;
+  if (m >= half_ring(W)) return W;  // full ring
+  return 2 * m + 1;
+}
+
+struct Workspace {
+  int32_t* mtab;      // [Hout][Hin]
+  int32_t* ringcnt;   // [Hout][Hin][R]
+  double* hq;         // [Hout][Hin][R]
+  int32_t* rowsum;    // [Hout][3 + R]: len, runs, hval rows, ring counts
+  int32_t* off;       // [Hout][Hin]: entry offset of the run inside its row
+  int32_t* runidx;    // [Hout][Hin]
+  int32_t* csroff;    // [Hout][Hin][R]
+  int32_t* hofftab;   // [Hout][Hin]
+  double* norm;       // [Hout][R]
+  int32_t* tcount;    // [Hin + 1]
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+size_t carve_workspace(const PsiGeom& g, char* base, Workspace* ws) {
+  size_t HH = (size_t)g.Hout * g.Hin, o = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + o : nullptr;
+    o += align256(bytes);
+    return p;
+  };
+  Workspace w;
+  w.mtab = (int32_t*)take(HH * 4);
+  w.ringcnt = (int32_t*)take(HH * g.R * 4);
+  w.hq = (double*)take(HH * g.R * 8);
+  w.rowsum = (int32_t*)take((size_t)g.Hout * (3 + g.R) * 4);
+  w.off = (int32_t*)take(HH * 4);
+  w.runidx = (int32_t*)take(HH * 4);
+  w.csroff = (int32_t*)take(HH * g.R * 4);
+  w.hofftab = (int32_t*)take(HH * 4);
+  w.norm = (double*)take((size_t)g.Hout * g.R * 8);
+  w.tcount = (int32_t*)take((size_t)(g.Hin + 1) * 4);
+  if (ws) *ws = w;
+  return o;
+}
+
+// ------------------------------------------------------------- kernels --
+
+// One block per output row; threads stride over input rows.
+__global__ void count_kernel(PsiGeom g, Workspace ws) {
+  int ho = blockIdx.x;
+  double th_o = colat(g.Hout, g.pout, ho);
+  for (int hi = threadIdx.x; hi < g.Hin; hi += blockDim.x) {
+    size_t t = (size_t)ho * g.Hin + hi;
+    double th_i = colat(g.Hin, g.pin, hi);
+    double q = quadw(g.Hin, g.pin, hi);
+    int cnt[kMaxRad] = {0};
+    double hqs[kMaxRad] = {0};
+    int m = -1;
+    if (fabs(__dsub_rn(th_i, th_o)) <= g.cutoff + 1e-9) {
+      int hr = half_ring(g.Win);
+      for (int ad = 0; ad <= hr; ++ad) {
+        double h[kMaxRad], d, beta;
+        bool st[kMaxRad];
+        if (!support_at(g, th_o, th_i, q, ad, h, st, &d, &beta)) break;
+        m = ad;
+        int mu = mult_at(ad, g.Win);
+        for (int r = 0; r < g.R; ++r)
+          if (st[r]) {
+            cnt[r] += mu;
+            double hq = __dmul_rn(h[r], q);
+            hqs[r] = __dadd_rn(hqs[r], hq);
+            if (mu == 2) hqs[r] = __dadd_rn(hqs[r], hq);
+          }
+      }
+    }
+    ws.mtab[t] = m;
+    for (int r = 0; r < g.R; ++r) {
+      ws.ringcnt[t * g.R + r] = cnt[r];
+      ws.hq[t * g.R + r] = hqs[r];
+    }
+  }
+}
+
+// One thread per output row: per-row totals (sequential over hi).
+__global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
+  int ho = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ho >= g.Hout) return;
+  int len = 0, runs = 0, hrows = 0, rc[kMaxRad] = {0};
+  for (int hi = 0; hi < g.Hin; ++hi) {
+    size_t t = (size_t)ho * g.Hin + hi;
+    int m = ws.mtab[t];
+    if (m < 0) continue;
+    len += run_len(m, g.Win);
+    runs += 1;
+    hrows += m + 1;  // pair steps delta = 0 .. m (m = W/2 includes the antipodal step)
+    for (int r = 0; r < g.R; ++r) rc[r] += ws.ringcnt[t * g.R + r];
+  }
+  int32_t* o = ws.rowsum + (size_t)ho * (3 + g.R);
+  o[0] = len;
+  o[1] = runs;
+  o[2] = hrows;
+  for (int r = 0; r < g.R; ++r) o[3 + r] = rc[r];
+}
+
+struct PsiOut {
+  int32_t *row_ptr, *idx, *csr_row_ptr, *csr_col, *run_ptr, *trun_ptr, *truns, *row_order;
+  float *val, *csr_val, *hval;
+  disco_run* runs;
+};
+
+__device__ __forceinline__ int ring_of(int kind, int k) { return kind == 1 ? k / 3 : k; }
+
+// Single thread: prefix sums over output rows (and over (k, ho) for CSR).
+__global__ void scan_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int32_t e = 0, r = 0;
+  p.row_ptr[0] = 0;
+  p.run_ptr[0] = 0;
+  for (int ho = 0; ho < g.Hout; ++ho) {
+    const int32_t* o = ws.rowsum + (size_t)ho * (3 + g.R);
+    e += o[0];
+    r += o[1];
+    p.row_ptr[ho + 1] = e;
+    p.run_ptr[ho + 1] = r;
+  }
+  int32_t c = 0;
+  p.csr_row_ptr[0] = 0;
+  for (int k = 0; k < g.K; ++k)
+    for (int ho = 0; ho < g.Hout; ++ho) {
+      c += ws.rowsum[(size_t)ho * (3 + g.R) + 3 + ring_of(g.kind, k)];
+      p.csr_row_ptr[k * g.Hout + ho + 1] = c;
+    }
+}
+
+// One thread per output row: offsets of each run inside the global arrays,
+// and the per-ring normalisers (summed over input rows in ascending order).
+__global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  int ho = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ho >= g.Hout) return;
+  int32_t off = 0, run = p.run_ptr[ho];
+  // pair-weight rows: runs are numbered globally in (ho, hi) order, so the
+  // hval offset of a run is the running total over all earlier runs.
+  int32_t hoff = 0;
+  for (int h2 = 0; h2 < ho; ++h2) hoff += ws.rowsum[(size_t)h2 * (3 + g.R) + 2];
+  int32_t rc[kMaxRad] = {0};
+  double nrm[kMaxRad] = {0};
+  for (int hi = 0; hi < g.Hin; ++hi) {
+    size_t t = (size_t)ho * g.Hin + hi;
+    int m = ws.mtab[t];
+    ws.off[t] = off;
+    ws.runidx[t] = m >= 0 ? run : -1;
+    ws.hofftab[t] = hoff;
+    for (int r = 0; r < g.R; ++r) ws.csroff[t * g.R + r] = rc[r];
+    if (m < 0) continue;
+    off += run_len(m, g.Win);
+    run += 1;
+    hoff += m + 1;
+    for (int r = 0; r < g.R; ++r) {
+      rc[r] += ws.ringcnt[t * g.R + r];
+      nrm[r] = __dadd_rn(nrm[r], ws.hq[t * g.R + r]);
+    }
+  }
+  for (int r = 0; r < g.R; ++r) ws.norm[(size_t)ho * g.R + r] = nrm[r];
+}
+
+// One block per output row; threads stride over input rows; each thread
+// writes one whole run in neighbour order.
+__global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  int ho = blockIdx.x;
+  double th_o = colat(g.Hout, g.pout, ho);
+  double nrm[kMaxRad];
+  for (int r = 0; r < g.R; ++r) nrm[r] = ws.norm[(size_t)ho * g.R + r];
+  for (int hi = threadIdx.x; hi < g.Hin; hi += blockDim.x) {
+    size_t t = (size_t)ho * g.Hin + hi;
+    int m = ws.mtab[t];
+    if (m < 0) continue;
+    double th_i = colat(g.Hin, g.pin, hi);
+    double q = quadw(g.Hin, g.pin, hi);
+    int W = g.Win, hr = half_ring(W);
+    int len = run_len(m, W);
+    bool full = (len == W);
+    int dlo = full ? -hr : -m;
+    int npair = full ? ((W % 2 == 0) ? hr - 1 : hr) : m;
+    int anti = (full && W % 2 == 0) ? 1 : 0;
+    int32_t e0 = p.row_ptr[ho] + ws.off[t];
+    int32_t hoff = ws.hofftab[t];
+    disco_run run;
+    run.ho = ho;
+    run.hi = hi;
+    run.D = npair + anti;
+    run.hoff = hoff;
+    run.e0 = e0;
+    run.len = len;
+    run.npair = npair;
+    run.anti = anti;
+    p.runs[ws.runidx[t]] = run;
+    int32_t rpos[kMaxRad];
+    for (int r = 0; r < g.R; ++r) rpos[r] = ws.csroff[t * g.R + r];
+    for (int j = 0; j < len; ++j) {
+      int delta = dlo + j;
+      int wi = delta < 0 ? delta + W : delta;
+      int64_t e = (int64_t)e0 + j;
+      double h[kMaxRad], d, beta;
+      bool st[kMaxRad];
+      support_at(g, th_o, th_i, q, delta < 0 ? -delta : delta, h, st, &d, &beta);
+      // bearing needs the signed offset
+      geometry(th_o, th_i, delta, W, &d, &beta);
+      p.idx[2 * e] = hi;
+      p.idx[2 * e + 1] = wi;
+      float vals[16];
+      for (int k = 0; k < g.K; ++k) {
+        int r = ring_of(g.kind, k), a = g.kind == 1 ? k % 3 : 0;
+        double v = 0.0;
+        if (st[r] && nrm[r] > 0.0) {
+          double ang = 1.0;
+          if (a != 0) ang = (d < kCoincident) ? 0.0 : (a == 1 ? cos(beta) : sin(beta));
+          v = __ddiv_rn(__dmul_rn(__dmul_rn(h[r], ang), q), nrm[r]);
+        }
+        vals[k] = __double2float_rn(v);
+        p.val[e * g.Kp + k] = vals[k];
+        if (st[r]) {
+          int32_t pos = p.csr_row_ptr[k * g.Hout + ho] + rpos[r];
+          p.csr_col[pos] = hi * W + wi;
+          p.csr_val[pos] = vals[k];
+        }
+      }
+      for (int k = g.K; k < g.Kp; ++k) p.val[e * g.Kp + k] = 0.f;
+      for (int r = 0; r < g.R; ++r)
+        if (st[r]) rpos[r] += 1;
+      // pair weights: delta = 0 .. npair, then the antipodal column
+      int hrow = -1;
+      float scale = 1.f;
+      if (delta >= 0 && delta <= npair) {
+        hrow = hoff + delta;
+        if (delta == 0) scale = 0.5f;
+      } else if (anti && delta == -hr) {
+        hrow = hoff + npair + 1;
+        scale = 0.5f;
+      }
+      if (hrow >= 0) {
+        for (int k = 0; k < g.K; ++k) p.hval[(int64_t)hrow * g.Kp + k] = vals[k] * scale;
+        for (int k = g.K; k < g.Kp; ++k) p.hval[(int64_t)hrow * g.Kp + k] = 0.f;
+      }
+    }
+  }
+}
+
+// transposed run list: count per input row, scan, fill (ho ascending)
+__global__ void tcount_kernel(PsiGeom g, Workspace ws) {
+  int hi = blockIdx.x * blockDim.x + threadIdx.x;
+  if (hi >= g.Hin) return;
+  int c = 0;
+  for (int ho = 0; ho < g.Hout; ++ho) c += ws.mtab[(size_t)ho * g.Hin + hi] >= 0;
+  ws.tcount[hi] = c;
+}
+
+__global__ void tscan_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int32_t c = 0;
+  p.trun_ptr[0] = 0;
+  for (int hi = 0; hi < g.Hin; ++hi) {
+    c += ws.tcount[hi];
+    p.trun_ptr[hi + 1] = c;
+  }
+}
+
+__global__ void tfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  int hi = blockIdx.x * blockDim.x + threadIdx.x;
+  if (hi >= g.Hin) return;
+  int32_t pos = p.trun_ptr[hi];
+  for (int ho = 0; ho < g.Hout; ++ho) {
+    int32_t r = ws.runidx[(size_t)ho * g.Hin + hi];
+    if (r >= 0) p.truns[pos++] = r;
+  }
+}
+
+// launch order of output rows: descending union length, ties by row index
+__global__ void order_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  int ho = blockIdx.x * blockDim.x + threadIdx.x;
+  if (ho >= g.Hout) return;
+  int my = ws.rowsum[(size_t)ho * (3 + g.R)];
+  int rank = 0;
+  for (int h2 = 0; h2 < g.Hout; ++h2) {
+    int o = ws.rowsum[(size_t)h2 * (3 + g.R)];
+    rank += (o > my) || (o == my && h2 < ho);
+  }
+  p.row_order[rank] = ho;
+}
+
+int make_geom(const disco_grid* gi, const disco_grid* go, const disco_basis* b, PsiGeom* g) {
+  if (!gi || !go || !b) return fail(DISCO_ERR_INVALID_ARG, "null grid or basis");
+  if (gi->nlat < 2 || go->nlat < 2 || gi->nlon < 1 || go->nlon < 1)
+    return fail(DISCO_ERR_INVALID_ARG, "grid too small (nlat >= 2, nlon >= 1)");
+  if ((gi->poles && gi->nlat < 3) || (go->poles && go->nlat < 3))
+    return fail(DISCO_ERR_INVALID_ARG, "pole grid needs nlat >= 3");
+  if (gi->nlon % go->nlon != 0)
+    return fail(DISCO_ERR_UNSUPPORTED, "W_in (%d) must be a multiple of W_out (%d)", gi->nlon, go->nlon);
+  if (b->kind != 0 && b->kind != 1) return fail(DISCO_ERR_INVALID_ARG, "basis kind must be 0 or 1");
+  if (b->n_radial < 1 || b->n_radial > kMaxRad)
+    return fail(DISCO_ERR_UNSUPPORTED, "n_radial must be in [1, %d]", kMaxRad);
+  if (!(b->cutoff > 0.0) || !(b->cutoff < kPi))
+    return fail(DISCO_ERR_INVALID_ARG, "cutoff must be in (0, pi)");
+  int K = b->kind == 1 ? 3 * b->n_radial : b->n_radial;
+  if (K > 16) return fail(DISCO_ERR_UNSUPPORTED, "K = %d > 16", K);
+  if ((int64_t)gi->nlat * gi->nlon >= (int64_t)1 << 30)
+    return fail(DISCO_ERR_UNSUPPORTED, "input grid too large for int32 indices");
+  g->Hin = gi->nlat;
+  g->Win = gi->nlon;
+  g->pin = gi->poles ? 1 : 0;
+  g->Hout = go->nlat;
+  g->Wout = go->nlon;
+  g->pout = go->poles ? 1 : 0;
+  g->kind = b->kind;
+  g->R = b->n_radial;
+  g->K = K;
+  g->Kp = (K + 7) / 8 * 8;
+  g->cutoff = b->cutoff;
+  g->width = b->cutoff / (double)b->n_radial;
+  return DISCO_OK;
+}
+
+size_t carve_psi(const disco_psi* psi, char* base, PsiOut* out) {
+  int Hin = psi->grid_in.nlat, Hout = psi->grid_out.nlat;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + o : nullptr;
+    o += align256(bytes);
+    return p;
+  };
+  PsiOut p;
+  p.row_ptr = (int32_t*)take((size_t)(Hout + 1) * 4);
+  p.idx = (int32_t*)take((size_t)psi->nnz * 8);
+  p.val = (float*)take((size_t)psi->nnz * psi->K_pad * 4);
+  p.csr_row_ptr = (int32_t*)take(((size_t)psi->K * Hout + 1) * 4);
+  p.csr_col = (int32_t*)take((size_t)psi->nnz_csr * 4);
+  p.csr_val = (float*)take((size_t)psi->nnz_csr * 4);
+  p.run_ptr = (int32_t*)take((size_t)(Hout + 1) * 4);
+  p.runs = (disco_run*)take((size_t)psi->nruns * sizeof(disco_run));
+  p.trun_ptr = (int32_t*)take((size_t)(Hin + 1) * 4);
+  p.truns = (int32_t*)take((size_t)psi->nruns * 4);
+  p.hval = (float*)take((size_t)psi->nhval * psi->K_pad * 4);
+  p.row_order = (int32_t*)take((size_t)Hout * 4);
+  if (out) *out = p;
+  return o;
+}
+
+}  // namespace
+}  // namespace disco
+
+using namespace disco;
+
+extern "C" int disco_psi_workspace_bytes(const disco_grid* grid_in, const disco_grid* grid_out,
+                                         const disco_basis* basis, size_t* bytes) {
+  PsiGeom g;
+  int st = make_geom(grid_in, grid_out, basis, &g);
+  if (st) return st;
+  if (!bytes) return fail(DISCO_ERR_INVALID_ARG, "bytes is null");
+  *bytes = carve_workspace(g, nullptr, nullptr);
+  return DISCO_OK;
+}
+
+extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_out,
+                              const disco_basis* basis, void* workspace, size_t workspace_bytes,
+                              void* stream, disco_psi* psi) {
+  PsiGeom g;
+  int st = make_geom(grid_in, grid_out, basis, &g);
+  if (st) return st;
+  if (!psi) return fail(DISCO_ERR_INVALID_ARG, "psi is null");
+  if ((st = check_device())) return st;
+  size_t need = carve_workspace(g, nullptr, nullptr);
+  if (!workspace || workspace_bytes < need)
+    return fail(DISCO_ERR_WORKSPACE, "psi workspace needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(DISCO_ERR_ALIGNMENT, "psi workspace must be 256-byte aligned");
+  Workspace ws;
+  carve_workspace(g, (char*)workspace, &ws);
+  cudaStream_t s = (cudaStream_t)stream;
+  count_kernel<<<g.Hout, 128, 0, s>>>(g, ws);
+  if ((st = check_launch("psi count"))) return st;
+  rowsum_kernel<<<(g.Hout + 127) / 128, 128, 0, s>>>(g, ws);
+  if ((st = check_launch("psi rowsum"))) return st;
+  std::vector<int32_t> rs((size_t)g.Hout * (3 + g.R));
+  cudaError_t ce = cudaMemcpyAsync(rs.data(), ws.rowsum, rs.size() * 4, cudaMemcpyDeviceToHost, s);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+  if (ce != cudaSuccess) return fail(DISCO_ERR_CUDA, "psi plan copy: %s", cudaGetErrorString(ce));
+  int64_t nnz = 0, nruns = 0, nhval = 0, nnz_csr = 0;
+  int32_t max_row = 0;
+  for (int ho = 0; ho < g.Hout; ++ho) {
+    const int32_t* o = &rs[(size_t)ho * (3 + g.R)];
+    nnz += o[0];
+    nruns += o[1];
+    nhval += o[2];
+    if (o[0] > max_row) max_row = o[0];
+    for (int k = 0; k < g.K; ++k) nnz_csr += o[3 + (g.kind == 1 ? k / 3 : k)];
+  }
+  if (nnz >= ((int64_t)1 << 31) / 16 || nnz_csr >= ((int64_t)1 << 31))
+    return fail(DISCO_ERR_UNSUPPORTED, "psi too large for int32 offsets");
+  memset(psi, 0, sizeof(*psi));
+  psi->grid_in = *grid_in;
+  psi->grid_out = *grid_out;
+  psi->basis = *basis;
+  psi->K = g.K;
+  psi->K_pad = g.Kp;
+  psi->s = g.Win / g.Wout;
+  psi->max_row = max_row;
+  psi->nnz = nnz;
+  psi->nnz_csr = nnz_csr;
+  psi->nruns = nruns;
+  psi->nhval = nhval;
+  psi->bytes = carve_psi(psi, nullptr, nullptr);
+  return DISCO_OK;
+}
+
+extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (!psi) return fail(DISCO_ERR_INVALID_ARG, "psi is null");
+  PsiGeom g;
+  int st = make_geom(&psi->grid_in, &psi->grid_out, &psi->basis, &g);
+  if (st) return st;
+  if ((st = check_device())) return st;
+  if (psi->K != g.K || psi->K_pad != g.Kp || psi->bytes != carve_psi(psi, nullptr, nullptr))
+    return fail(DISCO_ERR_INVALID_ARG, "psi sizes do not match its grids (call disco_psi_plan)");
+  if (!buffer || bytes < psi->bytes)
+    return fail(DISCO_ERR_INVALID_ARG, "psi buffer needs %zu bytes", psi->bytes);
+  if (reinterpret_cast<uintptr_t>(buffer) & 255u)
+    return fail(DISCO_ERR_ALIGNMENT, "psi buffer must be 256-byte aligned");
+  size_t need = carve_workspace(g, nullptr, nullptr);
+  if (!workspace || workspace_bytes < need)
+    return fail(DISCO_ERR_WORKSPACE, "psi workspace needs %zu bytes", need);
+  Workspace ws;
+  carve_workspace(g, (char*)workspace, &ws);
+  PsiOut p;
+  carve_psi(psi, (char*)buffer, &p);
+  cudaStream_t s = (cudaStream_t)stream;
+  int tb = 128;
+  scan_kernel<<<1, 1, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi scan"))) return st;
+  offsets_kernel<<<(g.Hout + tb - 1) / tb, tb, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi offsets"))) return st;
+  fill_kernel<<<g.Hout, 64, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi fill"))) return st;
+  tcount_kernel<<<(g.Hin + tb - 1) / tb, tb, 0, s>>>(g, ws);
+  if ((st = check_launch("psi tcount"))) return st;
+  tscan_kernel<<<1, 1, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi tscan"))) return st;
+  tfill_kernel<<<(g.Hin + tb - 1) / tb, tb, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi tfill"))) return st;
+  order_kernel<<<(g.Hout + tb - 1) / tb, tb, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi order"))) return st;
+  psi->row_ptr = p.row_ptr;
+  psi->idx = p.idx;
+  psi->val = p.val;
+  psi->csr_row_ptr = p.csr_row_ptr;
+  psi->csr_col = p.csr_col;
+  psi->csr_val = p.csr_val;
+  psi->run_ptr = p.run_ptr;
+  psi->runs = p.runs;
+  psi->trun_ptr = p.trun_ptr;
+  psi->truns = p.truns;
+  psi->hval = p.hval;
+  psi->row_order = p.row_order;
+  return DISCO_OK;
+}

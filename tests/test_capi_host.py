@@ -1,0 +1,68 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every symbol include/disco.h declares; host-only validation
+returns the documented status without touching a device."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_spherical_convolution_gb300 import build
+    build.build()
+    import sparse_spherical_convolution_gb300 as d
+    return d
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "disco.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(disco_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    so = ctypes.CDLL(lib.library_path())
+    for name in declared:
+        assert hasattr(so, name), name
+    assert set(declared) == set(lib.EXPORTED_SYMBOLS)
+
+
+def test_version_and_error_string(lib):
+    assert lib.disco_version() >= 100
+    assert isinstance(lib.disco_last_error(), str)
+
+
+def test_workspace_bytes_host_validation(lib):
+    b = lib.disco_basis(1, 3, 3 * math.pi / 64)
+    n = lib.disco_psi_workspace_bytes((128, 256, 0), (64, 128, 0), b)
+    assert n > 0 and n % 256 == 0
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_psi_workspace_bytes((128, 250, 0), (64, 128, 0), b)   # W_in % W_out != 0
+    assert e.value.status == -2
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_psi_workspace_bytes((128, 256, 0), (64, 128, 0), lib.disco_basis(1, 6, 0.1))  # K = 18
+    assert e.value.status == -2
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_psi_workspace_bytes((128, 256, 0), (64, 128, 0), lib.disco_basis(0, 3, -1.0))
+    assert e.value.status == -1
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_psi_workspace_bytes((2, 8, 1), (2, 8, 1), lib.disco_basis(0, 3, 0.5))  # pole grid nlat < 3
+    assert e.value.status == -1
+
+
+def test_hot_calls_reject_unbuilt_psi_before_any_launch(lib):
+    empty = lib.disco_psi()
+    so = lib.load_library()
+    assert so.disco_fwd(ctypes.byref(empty), None, None, 1, 1, 1, None) == -1
+    assert "psi" in lib.disco_last_error()
+    assert so.disco_bwd(None, None, None, 1, 1, 1, None) == -1
+    assert so.disco_fused_conv(ctypes.byref(empty), None, None, None, 1, 16, 16, 1, None) == -1
+    assert so.disco_fused_conv_bwd_input(ctypes.byref(empty), None, None, None, 1, 16, 16, 1,
+                                         None, 0, None) == -1

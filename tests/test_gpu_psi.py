@@ -1,0 +1,94 @@
+"""psi built on the GPU against the oracle: index structures bit-exact,
+values within 1 fp32 ulp of the fp64 oracle rounded to fp32."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_spherical_convolution_gb300.workloads import WORKLOADS
+from tests._helpers import ulp_diff_f32
+
+pytestmark = pytest.mark.gpu
+
+CASES = [(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff) for w in WORKLOADS.values()] + [
+    ((9, 16, 1), (9, 16, 1), 1, 3, 2 * math.pi / 8),       # coarse pole grid, empty ring at the pole
+    ((17, 32, 1), (9, 16, 1), 1, 2, 3 * math.pi / 8),      # s = 2, pole grids
+    ((12, 24, 0), (12, 24, 0), 1, 3, 4 * math.pi / 12),    # ties at d = cutoff on the meridian
+    ((10, 24, 0), (10, 12, 0), 0, 1, 0.9),                 # K = 1, W_out not a multiple of 8
+    ((16, 31, 0), (16, 31, 0), 0, 2, 2 * math.pi / 16),    # odd ring width
+]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_spherical_convolution_gb300 import build
+    build.build()
+    import sparse_spherical_convolution_gb300 as d
+    return d
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}->{c[1]}-k{c[2]}r{c[3]}")
+def test_psi_bit_exact(lib, case):
+    gi, go, kind, nrad, cut = case
+    ref = oracle.build_psi(gi, go, kind, nrad, cut)
+    psi = lib.Psi(gi, go, kind, nrad, cut)
+    torch.cuda.synchronize()
+    c = psi.c
+    assert c.K == ref.K and c.nnz == ref.row_ptr[-1] and c.nnz_csr == ref.csr_row_ptr[-1]
+    assert np.array_equal(psi.tensor("row_ptr").cpu().numpy(), ref.row_ptr)
+    assert np.array_equal(psi.tensor("idx").cpu().numpy(), ref.idx)
+    assert np.array_equal(psi.tensor("csr_row_ptr").cpu().numpy(), ref.csr_row_ptr)
+    assert np.array_equal(psi.tensor("csr_col").cpu().numpy(), ref.csr_col)
+    val = psi.tensor("val").cpu().numpy()
+    assert np.all(val[:, ref.K:] == 0)
+    assert ulp_diff_f32(val[:, :ref.K], ref.val.astype(np.float32)) <= 1
+    assert ulp_diff_f32(psi.tensor("csr_val").cpu().numpy(), ref.csr_val.astype(np.float32)) <= 1
+
+
+@pytest.mark.parametrize("case", CASES[:2] + CASES[5:], ids=lambda c: f"{c[0]}->{c[1]}")
+def test_runs_are_consistent_with_union_layout(lib, case):
+    """The kernel-side run table, transposed runs and pair weights describe
+    exactly the union layout."""
+    gi, go, kind, nrad, cut = case
+    psi = lib.Psi(gi, go, kind, nrad, cut)
+    torch.cuda.synchronize()
+    c = psi.c
+    W = gi[1]
+    row_ptr = psi.tensor("row_ptr").cpu().numpy()
+    idx = psi.tensor("idx").cpu().numpy()
+    val = psi.tensor("val").cpu().numpy()
+    runs = psi.tensor("runs").cpu().numpy()
+    run_ptr = psi.tensor("run_ptr").cpu().numpy()
+    hval = psi.tensor("hval").cpu().numpy()
+    covered = 0
+    for ho in range(go[0]):
+        rs = runs[run_ptr[ho]:run_ptr[ho + 1]]
+        assert np.all(rs[:, 0] == ho) and np.all(np.diff(rs[:, 1]) > 0)
+        e = row_ptr[ho]
+        for (rho, hi, D, hoff, e0, ln, npair, anti) in rs:
+            assert e0 == e
+            seg = idx[e0:e0 + ln]
+            assert np.all(seg[:, 0] == hi)
+            dl = ((seg[:, 1] + W // 2) % W) - W // 2
+            zero = e0 + int(np.where(dl == 0)[0][0])
+            for d in range(npair + 1):
+                scale = 0.5 if d == 0 else 1.0
+                assert np.array_equal(hval[hoff + d], val[zero + d] * scale)
+            if anti:
+                assert np.array_equal(hval[hoff + npair + 1], val[e0] * 0.5)
+            assert D == npair + anti
+            e += ln
+        covered += e - row_ptr[ho]
+        assert e == row_ptr[ho + 1]
+    assert covered == c.nnz
+    trun_ptr = psi.tensor("trun_ptr").cpu().numpy()
+    truns = psi.tensor("truns").cpu().numpy()
+    for hi in range(gi[0]):
+        rs = runs[truns[trun_ptr[hi]:trun_ptr[hi + 1]]]
+        assert np.all(rs[:, 1] == hi) and np.all(np.diff(rs[:, 0]) > 0)
+    order = psi.tensor("row_order").cpu().numpy()
+    assert sorted(order.tolist()) == list(range(go[0]))
+    work = np.diff(row_ptr)[order]
+    assert np.all(np.diff(work) <= 0)
