@@ -1,0 +1,377 @@
+"""Benchmark of the DISCO hot path on one or more GPUs (replicas).
+
+One step = the whole hot path on one batch of the largest workload
+(B=1, C=256 -> 256, 721x1440 -> 361x720, K=9 anisotropic, bf16):
+disco_fwd (x -> X), disco_bwd (G -> gx), disco_fused_conv (x, W -> y) and
+disco_fused_conv_bwd_input (dy, W -> gx).  The metric is the forward +
+transpose contraction throughput in algorithmic HBM GB/s (compulsory bytes:
+input + output + psi), with the fused convolution's ms/call alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica (no data-path
+collective; the path shards by batch), timing is max over ranks and rank 0
+prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "down_fused_bwd_721x1440_to_361x720"
+METRIC = "DISCO fwd/bwd contraction HBM GB/s (% of peak); fused conv ms/call"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic(w, psi_c):
+    """Compulsory bytes and useful flops per call (see the design notes)."""
+    esz = 2 if w.dtype == "bf16" else 4
+    B, C, K = w.B, w.C, w.K
+    Hin, Win = w.grid_in[:2]
+    Hout, Wout = w.grid_out[:2]
+    x = B * C * Hin * Win * esz
+    X = B * C * K * Hout * Wout * esz
+    psi = psi_c.nruns * 32 + psi_c.nhval * psi_c.K_pad * 4 + (Hout + 1) * 8
+    out = {"fwd_bytes": x + X + psi, "bwd_bytes": X + x + psi,
+           "csr_flops": 2.0 * B * C * Wout * psi_c.nnz_csr}
+    if w.Cout is not None:
+        y = B * w.Cout * Hout * Wout * esz
+        Wb = w.Cout * C * K * esz
+        out["fused_bytes"] = x + Wb + y + psi
+        out["fused_bwd_bytes"] = y + Wb + x + psi
+        out["einsum_flops"] = 2.0 * B * w.Cout * C * K * Hout * Wout
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import sparse_spherical_convolution_gb300 as d
+    from sparse_spherical_convolution_gb300.workloads import WORKLOADS
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    d.load_library()
+    psi = d.Psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
+    B, C, Co, K = w.B, w.C, w.Cout, w.K
+    sh = w.shapes()
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed * 1000 + rank)
+    dt = w.torch_dtype
+    x = torch.randn(sh["x"], generator=g, device=dev).to(dt)
+    G = torch.randn(sh["X"], generator=g, device=dev).to(dt)
+    Wt = (torch.randn(sh["W"], generator=g, device=dev) / math.sqrt(C * K)).to(dt)
+    dy = torch.randn(sh["y"], generator=g, device=dev).to(dt)
+    X = torch.empty(sh["X"], dtype=dt, device=dev)
+    gx = torch.empty(sh["x"], dtype=dt, device=dev)
+    y = torch.empty(sh["y"], dtype=dt, device=dev)
+    gx2 = torch.empty(sh["x"], dtype=dt, device=dev)
+    wsb = d.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, C)
+    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    alg = algorithmic(w, psi.c)
+
+    calls = [
+        ("fwd", lambda: d.disco_fwd(psi.c, x, X, B, C, stream)),
+        ("bwd", lambda: d.disco_bwd(psi.c, G, gx, B, C, stream)),
+        ("fused", lambda: d.disco_fused_conv(psi.c, x, Wt, y, B, C, Co, stream)),
+        ("fused_bwd", lambda: d.disco_fused_conv_bwd_input(psi.c, dy, Wt, gx2, B, C, Co, wsp, stream)),
+    ]
+    launches_per_step = 5  # fwd, bwd, fused, dX gemm + transpose
+
+    def step(ev=None):
+        for i, (_, fn) in enumerate(calls):
+            if ev is not None:
+                ev[i][0].record(stream)
+            fn()
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if d.disco_device_status() != 0:
+        raise RuntimeError("a bounded wait timed out during warm-up")
+
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in calls] for _ in range(args.steps)]
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0e.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1e.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    total_ms = t0e.elapsed_time(t1e)
+    per = {name: [evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)]
+           for i, (name, _) in enumerate(calls)}
+    contr_ms = sum(per["fwd"]) + sum(per["bwd"])
+    if ws > 1:
+        tt = torch.tensor([total_ms, contr_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms, contr_ms = float(tt[0]), float(tt[1])
+    if d.disco_device_status() != 0:
+        raise RuntimeError("a bounded wait timed out during the timed region")
+
+    # end to end through the C ABI with host buffers: pinned inputs in,
+    # results out, copies inside the timed region
+    e2e = None
+    if rank == 0 or ws > 1:
+        xh = x.cpu().pin_memory()
+        Gh = G.cpu().pin_memory()
+        Xh = torch.empty(sh["X"], dtype=dt).pin_memory()
+        gxh = torch.empty(sh["x"], dtype=dt).pin_memory()
+        xd2, Gd2 = torch.empty_like(x), torch.empty_like(G)
+
+        def e2e_step():
+            xd2.copy_(xh, non_blocking=True)
+            Gd2.copy_(Gh, non_blocking=True)
+            d.disco_fwd(psi.c, xd2, X, B, C, stream)
+            d.disco_bwd(psi.c, Gd2, gx, B, C, stream)
+            Xh.copy_(X, non_blocking=True)
+            gxh.copy_(gx, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        ne = max(1, min(args.steps, 5))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / ne
+        if ws > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt[0])
+        e2e = {"value": round(ws * (alg["fwd_bytes"] + alg["bwd_bytes"]) / (e2e_ms * 1e6), 2),
+               "unit": "GB/s",
+               "h2d_bytes_per_step": x.numel() * x.element_size() + G.numel() * G.element_size(),
+               "d2h_bytes_per_step": X.numel() * X.element_size() + gx.numel() * gx.element_size(),
+               "ms_per_step": round(e2e_ms, 3)}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    peaks, peak_src = _peaks()
+    value = ws * (alg["fwd_bytes"] + alg["bwd_bytes"]) * args.steps / (contr_ms * 1e6)
+    med = {k: statistics.median(v) for k, v in per.items()}
+    share = {k: sum(v) for k, v in per.items()}
+    dom = max(share, key=share.get)
+    clocks = clk.summary()
+    # dominant kernel: plain FP32 FMA arithmetic (CUDA cores); peak = SMs x
+    # 128 FP32 lanes x 2 flops x the measured median SM clock under load
+    sm_mhz = clocks["sm_mhz"] or peaks.get("sm_max_mhz", 2070.0)
+    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+    dom_flops = alg["csr_flops"]  # fwd, bwd and the fused gather share the CSR FMA count
+    achieved = dom_flops / (med[dom] * 1e-3) / 1e12
+    traffic = _traffic_from_profiles(dom)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, W ~ N(0, 1/(Cin*K)))",
+        "config": {"workload": w.name, "B": w.B, "Cin": w.C, "Cout": w.Cout,
+                   "grid_in": list(w.grid_in), "grid_out": list(w.grid_out), "K": w.K,
+                   "basis": "anisotropic 3 radial hats x {1, cos, sin}", "cutoff_rad": w.cutoff,
+                   "step": "disco_fwd + disco_bwd + disco_fused_conv + disco_fused_conv_bwd_input",
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{ws}"},
+        "hbm_frac_of_measured_peak": round(value / ws / peaks["hbm_gbs"], 4),
+        "fused_conv_ms_per_call": round(med["fused"], 3),
+        "fused_conv_bwd_input_ms_per_call": round(med["fused_bwd"], 3),
+        "kernel_ms": {k: round(v, 3) for k, v in med.items()},
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2),
+                     "peak": round(alu_peak, 2), "unit": "TFLOP/s",
+                     "frac": round(achieved / alu_peak, 4), "traffic": traffic,
+                     "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz (measured clock)"},
+        "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peak_src,
+        "clocks": clocks, "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch of `kernel`, taken from a committed ncu summary
+    (profiles/traffic.json) when it matches the current sources, else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(kernel)
+    except Exception:
+        return None
+
+
+def cpu_baseline(w, budget_s: float):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    the forward and transpose contractions over the first n channels (n =
+    host cores, one OpenMP thread each), scaled to the same GB/s metric."""
+    import numpy as np
+    import torch
+    import oracle
+    from sparse_spherical_convolution_gb300.workloads import WORKLOADS  # noqa: F401
+
+    cores = os.cpu_count() or 1
+    ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
+    g = torch.Generator().manual_seed(w.seed)
+    Hin, Win = w.grid_in[:2]
+    Hout, Wout = w.grid_out[:2]
+    n = max(1, min(w.C, cores))
+    x = torch.randn((1, n, Hin, Win), generator=g).to(torch.bfloat16).double().numpy()
+    G = torch.randn((1, n, w.K, Hout, Wout), generator=g).to(torch.bfloat16).double().numpy()
+    t0 = time.perf_counter()
+    oracle.fwd(ref, x)
+    t1 = time.perf_counter()
+    oracle.bwd(ref, G)
+    t2 = time.perf_counter()
+    esz = 2
+    frac = n / w.C
+    byts = (x.size + G.size) * esz * 2  # fwd + bwd, input + output, for the sample
+    del np
+    return {"value": round(byts / (t2 - t0) / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"fp64 oracle fwd + bwd over {n} of {w.C} channels ({frac:.3f} of the "
+                      f"workload), {t1 - t0:.1f} s + {t2 - t1:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from sparse_spherical_convolution_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    vals = []
+    cb = None
+    for _ in range(args.warmup):
+        cpu_baseline(w, args.cpu_budget_s)
+    for _ in range(args.steps):
+        cb = cpu_baseline(w, args.cpu_budget_s)
+        vals.append(cb["value"])
+    v = statistics.median(vals)
+    out = {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+           "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": w.name, "step": "fp64 CPU oracle fwd + bwd on a channel sample"},
+           "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cb["cores"], "kind": "oracle",
+                            "sample": cb["sample"]},
+           "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -201,6 +201,13 @@ DISCO_API int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, c
                                disco_dtype dtype, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
+   the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
+   of the fused forward timed out, bit 1 = one of the dX GEMM timed out; a
+   kernel that times out stops issuing work, frees its tensor memory and
+   returns, leaving its outputs incomplete).  clear != 0 resets the word. */
+DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
+
 #ifdef __cplusplus
 }
 #endif

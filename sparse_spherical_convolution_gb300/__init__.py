@@ -20,7 +20,7 @@ __all__ = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
     "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
-    "library_path", "load_library", "EXPORTED_SYMBOLS",
+    "disco_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
 ]
 
 DISCO_F32, DISCO_BF16 = 0, 1
@@ -101,6 +101,8 @@ def load_library():
     lib.disco_fused_conv_bwd_input_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
     lib.disco_fused_conv_bwd_input.restype = ctypes.c_int
     lib.disco_fused_conv_bwd_input.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
+    lib.disco_device_status.restype = ctypes.c_int
+    lib.disco_device_status.argtypes = [ctypes.POINTER(I32), I32]
     _lib = lib
     return lib
 
@@ -204,6 +206,13 @@ def disco_fused_conv_bwd_input(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout
         ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy),
         _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
         _stream(stream)))
+
+
+def disco_device_status(clear: bool = True) -> int:
+    """Device status word (0 = no bounded wait timed out); synchronises the device."""
+    v = ctypes.c_int32()
+    _check(load_library().disco_device_status(ctypes.byref(v), 1 if clear else 0))
+    return v.value
 
 
 # ------------------------------------------------------------ convenience

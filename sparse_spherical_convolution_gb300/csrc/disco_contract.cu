@@ -23,7 +23,7 @@
 //    keeps K x 8 fp32 accumulators in registers.
 //  * Blocks of the forward are launched heaviest output rows first (psi.row_order).
 
-#include "disco_internal.cuh"
+#include "disco_gather.cuh"
 
 namespace disco {
 namespace {
@@ -31,7 +31,6 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kTW = 8;         // output columns per thread
 constexpr int kTile = 64;      // output columns per block
-constexpr int kDCMax = 32;     // pair steps per staged chunk
 
 struct ContractArgs {
   const void* in;
@@ -45,11 +44,6 @@ struct ContractArgs {
   const int32_t* row_order;
   int vec_ok;  // output rows are 16-byte aligned
 };
-
-__device__ __forceinline__ int imod(int a, int m) {
-  int r = a % m;
-  return r < 0 ? r + m : r;
-}
 
 template <typename T>
 __device__ __forceinline__ float ld_in(const T* p) {
@@ -87,104 +81,34 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const 
   }
 }
 
-// window lengths (columns per channel) of the two staging modes
-template <int S>
-struct Win {
-  static constexpr int kSingle = S * (kTile - 1) + 2 * kDCMax - 1;  // chunk 0: both sides
-  static constexpr int kDouble = S * (kTile - 1) + kDCMax;          // later chunks: per side
-  static constexpr int kLen = (kSingle > 2 * kDouble) ? kSingle : 2 * kDouble;
-};
-
 // ------------------------------------------------------------- forward --
 //
 // X[bc,k,ho,wo] = sum_runs sum_{delta=0..D} w_k(delta) * (x[hi, S wo + delta] +/- x[hi, S wo - delta])
+// Lane = channel (32 per block), warp = 8 consecutive output columns.
+template <typename T, int K, int S, bool ANISO>
+using FwdGather = RowGather<T, K, S, ANISO, 32, kTW, kTile, kThreads>;
+
 template <typename T, int K, int S, bool ANISO>
 __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const ContractArgs a) {
   extern __shared__ float sm[];
-  // layout: window rows [32][pitch] (pitch odd), then pair weights [kDCMax][K]
-  constexpr int kPitch = Win<S>::kLen | 1;
-  float* win = sm;
-  float* wts = sm + 32 * kPitch;
-
+  using G = FwdGather<T, K, S, ANISO>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ho = a.row_order[blockIdx.z];
   const int bc0 = blockIdx.y * 32;
   const int wo_blk = blockIdx.x * kTile;
-  const int o0 = warp * kTW;  // first output column of this thread inside the tile
-  const T* x = reinterpret_cast<const T*>(a.in);
-  const int W = a.Win;
-  const int P0 = S * wo_blk;  // input column of output column wo_blk at offset 0
-
+  const int o0 = warp * kTW;
+  typename G::Args ga;
+  ga.x = reinterpret_cast<const T*>(a.in);
+  ga.bc0 = bc0;
+  ga.BC = a.BC;
+  ga.Hin = a.Hin;
+  ga.W = a.Win;
+  ga.run_ptr = a.run_ptr;
+  ga.runs = a.runs;
+  ga.hval = a.hval;
+  ga.Kp = a.Kp;
   float acc[K][kTW];
-#pragma unroll
-  for (int k = 0; k < K; ++k)
-#pragma unroll
-    for (int t = 0; t < kTW; ++t) acc[k][t] = 0.f;
-
-  const int r_begin = a.run_ptr[ho], r_end = a.run_ptr[ho + 1];
-  for (int r = r_begin; r < r_end; ++r) {
-    const disco_run run = a.runs[r];
-    const int steps = run.D + 1;
-    const int dc = min(kDCMax, (steps + 7) & ~7);
-    for (int da = 0; da < steps; da += dc) {
-      const int nd = min(dc, steps - da);
-      const bool single = (da == 0);
-      // plus side reads window index S*o + offp + u, minus side S*o + offm - u
-      const int len_p = single ? S * (kTile - 1) + 2 * dc - 1 : S * (kTile - 1) + dc;
-      const int start_p = single ? P0 - (dc - 1) : P0 + da;          // first column of window 0
-      const int start_m = P0 - da - (dc - 1);                        // first column of window 1
-      const int offp = single ? dc - 1 : 0;
-      const int offm = dc - 1;
-      float* wp = win;
-      float* wm = single ? win : win + len_p;
-      __syncthreads();
-      {
-        const int nwin = single ? 1 : 2;
-        const int total = 32 * len_p * nwin;
-        const int sp = imod(start_p, W), smn = imod(start_m, W);
-        for (int i = threadIdx.x; i < total; i += kThreads) {
-          int w2 = i / (32 * len_p);
-          int rem = i - w2 * 32 * len_p;
-          int c = rem / len_p, j = rem - c * len_p;
-          int col = ((w2 ? smn : sp) + j) % W;
-          int bc = bc0 + c;
-          float v = 0.f;
-          if (bc < a.BC) v = ld_in(x + ((size_t)bc * a.Hin + run.hi) * W + col);
-          win[c * kPitch + w2 * len_p + j] = v;
-        }
-        for (int i = threadIdx.x; i < dc * K; i += kThreads) {
-          int u = i / K, k = i - u * K;
-          wts[i] = (u < nd) ? a.hval[(size_t)(run.hoff + da + u) * a.Kp + k] : 0.f;
-        }
-      }
-      __syncthreads();
-      const float* bp = wp + lane * kPitch + S * o0 + offp;
-      const float* bm = wm + lane * kPitch + S * o0 + offm;
-      for (int ub = 0; ub < nd; ub += 8) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float w[K];
-#pragma unroll
-          for (int k = 0; k < K; ++k) w[k] = wts[(ub + u) * K + k];
-#pragma unroll
-          for (int t = 0; t < kTW; ++t) {
-            const float xp = bp[ub + S * t + u];
-            const float xm = bm[-ub + S * t - u];
-            const float pp = xp + xm;
-            if (ANISO) {
-              const float qq = xp - xm;
-#pragma unroll
-              for (int k = 0; k < K; ++k)
-                acc[k][t] = fmaf(w[k], (k % 3 == 2) ? qq : pp, acc[k][t]);
-            } else {
-#pragma unroll
-              for (int k = 0; k < K; ++k) acc[k][t] = fmaf(w[k], pp, acc[k][t]);
-            }
-          }
-        }
-      }
-    }
-  }
+  G::run(acc, sm, ga, ho, wo_blk, lane, o0, threadIdx.x, 0);
 
   const int bc = bc0 + lane;
   const int wo = wo_blk + o0;
@@ -299,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) 
   store8<T>(gx + ((size_t)bc * a.Hin + hi) * a.Win + wi, acc, n, a.vec_ok != 0);
 }
 
-template <int S>
-constexpr size_t fwd_smem(int K) {
-  return (size_t)(32 * (Win<S>::kLen | 1) + kDCMax * K) * sizeof(float);
+template <typename T, int K, int S, bool ANISO>
+constexpr size_t fwd_smem() {
+  return (size_t)FwdGather<T, K, S, ANISO>::kSmemFloats * sizeof(float);
 }
 template <int S>
 constexpr size_t bwd_smem() {
@@ -311,7 +235,7 @@ constexpr size_t bwd_smem() {
 template <typename T, int K, int S, bool ANISO>
 int launch_fwd(const ContractArgs& a, cudaStream_t st) {
   auto kern = fwd_kernel<T, K, S, ANISO>;
-  size_t smem = fwd_smem<S>(K);
+  size_t smem = fwd_smem<T, K, S, ANISO>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return check_launch("disco_fwd attribute");
