@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
     "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
+    "disco_device_status",
 ]
 
 
