@@ -160,7 +160,9 @@ DISCO_API int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes
      X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]
                         * x[b,c,hi,(wi + wo*s) mod W_in]
    x: [B, C, H_in, W_in], X: [B, C, K, H_out, W_out], both `dtype`.
-   Supports s in {1, 2}; W_out % 8 == 0 for bf16 and % 4 == 0 for fp32. */
+   Supports s in {1, 2}.  bf16 with W_in % 8 == 0 runs on the tensor cores
+   (banded Toeplitz tiles of the run windows, fp32 accumulation in tensor
+   memory); fp32, and bf16 with other widths, run the CUDA-core gather. */
 DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
@@ -203,7 +205,8 @@ DISCO_API int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, c
 
 /* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
-   of the fused forward timed out, bit 1 = one of the dX GEMM timed out; a
+   of the fused forward timed out, bit 1 = one of the dX GEMM timed out,
+   bit 2 = one of the tensor-core forward contraction timed out; a
    kernel that times out stops issuing work, frees its tensor memory and
    returns, leaving its outputs incomplete).  clear != 0 resets the word. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);

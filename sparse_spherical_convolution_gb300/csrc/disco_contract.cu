@@ -176,18 +176,21 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) 
         float* wp = single ? win : win + len_p;
         __syncthreads();
         {
-          const int nwin = single ? 1 : 2;
-          const int total = 32 * len_p * nwin;
+          // one warp per window row (channel x side), lanes along the columns
+          const int nrows = 32 * (single ? 1 : 2);
           const int smn = imod(start_m, Wo), sp = imod(start_p, Wo);
-          for (int i = threadIdx.x; i < total; i += kThreads) {
-            int w2 = i / (32 * len_p);
-            int rem = i - w2 * 32 * len_p;
-            int c = rem / len_p, j = rem - c * len_p;
-            int col = ((w2 ? sp : smn) + j) % Wo;
-            int bc = bc0 + c;
-            float v = 0.f;
-            if (bc < a.BC) v = ld_in(Gk + bc * plane + col);
-            win[c * kPitch + w2 * len_p + j] = v;
+          for (int row = threadIdx.x >> 5; row < nrows; row += kThreads / 32) {
+            const int w2 = row >= 32;
+            const int c = row - w2 * 32;
+            const int bc = bc0 + c;
+            const int base = w2 ? sp : smn;
+            float* dst = win + c * kPitch + w2 * len_p;
+            const T* src = Gk + bc * plane;
+            for (int j = lane; j < len_p; j += 32) {
+              int col = base + j;
+              if (col >= Wo) col %= Wo;
+              dst[j] = (bc < a.BC) ? ld_in(src + col) : 0.f;
+            }
           }
           for (int i = threadIdx.x; i < dc; i += kThreads)
             wts[i] = (i < nd) ? a.hval[(size_t)(run.hoff + da + i) * a.Kp + k] : 0.f;
@@ -307,6 +310,11 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   a.vec_ok = ((fwd ? a.Wout : a.Win) % elems16) == 0;
   cudaStream_t s = (cudaStream_t)stream;
   int kind = psi->basis.kind, K = psi->K;
+  if (fwd && dtype == DISCO_BF16) {
+    // bf16 forward: the tensor-core Toeplitz kernel where its shape rules hold
+    const int tst = fwd_tensor_core(psi, in, out, a.BC, s);
+    if (tst != DISCO_ERR_UNSUPPORTED) return tst;
+  }
   if (dtype == DISCO_F32)
     return psi->s == 1 ? dispatch<float, 1>(fwd, kind, K, a, s) : dispatch<float, 2>(fwd, kind, K, a, s);
   return psi->s == 1 ? dispatch<__nv_bfloat16, 1>(fwd, kind, K, a, s)

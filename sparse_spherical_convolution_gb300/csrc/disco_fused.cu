@@ -523,6 +523,7 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
     const int32_t zero = 0;
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int32_t));
   }
+  if (e == cudaSuccess) e = tc_status(flags, clear != 0);
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
   return DISCO_OK;
 }

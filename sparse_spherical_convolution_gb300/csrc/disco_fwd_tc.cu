@@ -1,0 +1,407 @@
+// disco_fwd_tc.cu -- the forward DISCO contraction on the tensor cores (bf16).
+//
+// DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
+// ("forward: CSR sparse contraction inp -> (B,C,K,H,W)") and §kpacked layout
+// (psi values of all K side by side, which is what lets a tensor-core tile
+// produce all basis functions at once; the page's WGMMA kernel is the Hopper
+// form of the same idea).
+//
+// For one run (output row ho, input row hi) the contraction over the run's
+// wrapped column window is a banded Toeplitz product.  For 16 consecutive
+// output columns wo = w0 + t,
+//
+//   X[bc, k, ho, w0 + t] += sum_u x[bc, hi, u0 + u] * T[u, k*16 + t],
+//   T[u, k*16 + t] = psi_k(delta = u - S*t - M)   (0 outside the run)
+//
+// with u0 = S*w0 - M and M = the run's half-width rounded up to 8, so that
+// every 8-column group of the window starts on a 16-byte boundary and never
+// straddles the longitude wrap.  That is an MMA with M = 128 channels,
+// N = 16*K, and a K extent of the window length:
+//   A = x window [128 channels x window columns]: TMA, one 2 KB box per
+//       8-column group, wrapped column index, rows beyond B*C zero-filled;
+//   B = T [16K x window columns], built in shared memory by 6 warps from the
+//       psi values of the run (bf16);
+//   D = X [128 channels x (k, t)] in TMEM, fp32, accumulated over all runs.
+// One CTA owns (ho, 128 channels, NT tiles of 16 columns); the window of NT
+// tiles is loaded once per 128-column chunk and shared by the NT MMAs (tile j
+// starts S*16*j columns further into it).  Two pipeline stages; roles:
+//   warp 0  TMA producer of A chunks (and TMEM owner)
+//   warp 1  MMA issuer (one thread)
+//   warps 2-7 build B chunks; warps 4-7 also run the epilogue
+//             (tcgen05.ld of 16 columns = 16 consecutive wo of one k,
+//              bf16 rounding, two 16-byte stores per thread).
+// All mbarrier waits are bounded (time-out -> device status flag, abort).
+
+#include <cudaTypedefs.h>
+
+#include "disco_internal.cuh"
+#include "disco_umma.cuh"
+
+namespace disco {
+
+// status word of this translation unit (bit 2: a bounded wait timed out)
+__device__ int g_tc_status = 0;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBuilderThreads = 192;   // warps 2..7
+constexpr int kTW = 16;                // output columns per MMA tile
+constexpr int kCK = 8;                 // K steps (16 window columns) per chunk
+constexpr int kChunkCols = kCK * 16;   // 128
+constexpr int kStages = 2;
+constexpr uint32_t kGroupBytes = 128 * 16;  // one TMA box: 128 rows x 8 bf16
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kStatusTcTimeout = 4;
+
+__device__ __forceinline__ void tc_flag(int bit) { atomicOr(&g_tc_status, bit); }
+
+__device__ __forceinline__ int wrap_col(int c, int W) {
+  int r = c % W;
+  return r < 0 ? r + W : r;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+struct TcArgs {
+  __nv_bfloat16* X;   // [BC][K][Hout][Wout]
+  const float* val;   // union layout values [nnz][Kp]
+  const disco_run* runs;
+  const int32_t* run_ptr;
+  const int32_t* row_order;
+  int BC, Hout, Wout, Win, Kp;
+};
+
+// geometry of one run for the Toeplitz tiles
+struct RunGeom {
+  int hi, e0, dlo, len, M, KS;
+};
+
+template <int S>
+__device__ __forceinline__ RunGeom run_geom(const disco_run& r, int Win) {
+  RunGeom g;
+  g.hi = r.hi;
+  g.e0 = r.e0;
+  g.len = r.len;
+  g.dlo = (r.len == Win) ? -(Win / 2) : -r.npair;
+  g.M = ((-g.dlo) + 7) & ~7;
+  const int L = S * (kTW - 1) + 2 * g.M + 1;
+  g.KS = (L + 15) >> 4;
+  return g;
+}
+
+template <int K, int S>
+struct TcCfg {
+  static constexpr int N = 16 * K;                      // MMA N
+  static constexpr uint32_t kBBytes = N * kChunkCols * 2;  // B chunk
+  static constexpr uint32_t kSBOB = (kChunkCols / 8) * 128;  // 2048
+  static constexpr int NT = (512 / N) < 4 ? (512 / N) : 4;  // tiles per CTA
+  static constexpr int AG = (kChunkCols + S * kTW * (NT - 1)) / 8;  // A groups per stage
+  static constexpr uint32_t kABytes = AG * kGroupBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = (NT * N <= 32) ? 32 : (NT * N <= 64) ? 64 : (NT * N <= 128) ? 128
+                                        : (NT * N <= 256) ? 256 : 512;
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 128;
+};
+
+template <int K, int S>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
+  using Cfg = TcCfg<K, S>;
+  constexpr int N = Cfg::N, NT = Cfg::NT;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
+  uint64_t* fullA = bars;          // [2] TMA bytes landed
+  uint64_t* fullB = bars + 2;      // [2] B chunk built (192 arrivals)
+  uint64_t* empty = bars + 4;      // [2] MMAs of the stage done (commit)
+  uint64_t* done = bars + 6;       // all MMAs done (commit)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ho = a.row_order[blockIdx.z];
+  const int bc0 = blockIdx.y * 128;
+  const int wc = blockIdx.x * (kTW * NT);
+  const int r_begin = a.run_ptr[ho], r_end = a.run_ptr[ho + 1];
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&fullA[s], 1);
+      mbar_init(&fullB[s], kBuilderThreads);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, Cfg::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // number of work items (run, chunk) of this row
+  int items = 0;
+  for (int r = r_begin; r < r_end; ++r) items += (run_geom<S>(a.runs[r], a.Win).KS + kCK - 1) / kCK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int i = 0;
+      bool aborted = false;
+      for (int r = r_begin; r < r_end && !aborted; ++r) {
+        const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+        const int u0 = S * wc - g.M;
+        for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+          const int s = i & 1;
+          if ((i >= kStages && !mbar_wait(&empty[s], ((i >> 1) - 1) & 1, kWaitLimit)) || *abort_flag) {
+            tc_flag(kStatusTcTimeout);
+            *abort_flag = 1;
+            aborted = true;
+            break;
+          }
+          const int nks = min(kCK, g.KS - c * kCK);
+          const int ng = (S * kTW * (NT - 1) + 16 * nks) / 8;
+          uint8_t* sA = smem + s * Cfg::kStageBytes;
+          mbar_expect_tx(&fullA[s], ng * kGroupBytes);
+          for (int gi = 0; gi < ng; ++gi) {
+            const int col = wrap_col(u0 + c * kChunkCols + 8 * gi, a.Win);
+            tma_load_3d(sA + gi * kGroupBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+          }
+        }
+      }
+      if (aborted) {
+        // let the copies this thread issued land (bounded) before the CTA exits
+        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
+          const int li = i - back;
+          mbar_wait(&fullA[li & 1], (li >> 1) & 1, kWaitLimit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N);
+      int i = 0;
+      bool ok = true;
+      for (int r = r_begin; r < r_end && ok; ++r) {
+        const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+        for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+          const int s = i & 1;
+          const uint32_t ph = (i >> 1) & 1;
+          if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) ||
+              *abort_flag) {
+            tc_flag(kStatusTcTimeout);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nks = min(kCK, g.KS - c * kCK);
+          const uint32_t abase = smem_u32(smem + s * Cfg::kStageBytes);
+          const uint32_t bbase = abase + Cfg::kABytes;
+          for (int j = 0; j < NT; ++j)
+            for (int ks = 0; ks < nks; ++ks) {
+              // A: LBO (next 8 columns) = one 2 KB group, SBO (next 8 rows) = 128 B
+              const uint64_t ad = smem_desc(abase + (uint32_t)(2 * S * j + 2 * ks) * kGroupBytes,
+                                            kGroupBytes, 128);
+              const uint64_t bd = smem_desc(bbase + ks * 256, 128, Cfg::kSBOB);
+              umma_bf16(tmem + j * N, ad, bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+            }
+          umma_commit(&empty[s]);
+        }
+      }
+      umma_commit(done);  // arrives when every MMA issued above has completed
+    }
+  } else {
+    // ------------------------------------------------- B builders (6 warps) --
+    const int btid = tid - 64;
+    int i = 0;
+    for (int r = r_begin; r < r_end; ++r) {
+      const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+      for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+        const int s = i & 1;
+        bool ok = true;
+        if (i >= kStages) ok = mbar_wait(&empty[s], ((i >> 1) - 1) & 1, kWaitLimit);
+        if (!ok || *abort_flag) {
+          if (!ok) tc_flag(kStatusTcTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* sB = smem + s * Cfg::kStageBytes + Cfg::kABytes;
+        const int nks = min(kCK, g.KS - c * kCK);
+        const int ngrp = 2 * nks;  // 8-column groups of this chunk
+        for (int idx = btid; idx < N * ngrp; idx += kBuilderThreads) {
+          const int n = idx % N, gi = idx / N;
+          const int k = n >> 4, t = n & 15;
+          const int d0 = c * kChunkCols + 8 * gi - S * t - g.M;  // offset delta of column 0 of the group
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float v0 = 0.f, v1 = 0.f;
+            const int q0 = d0 + e - g.dlo, q1 = q0 + 1;
+            if (q0 >= 0 && q0 < g.len) v0 = __ldg(a.val + (size_t)(g.e0 + q0) * a.Kp + k);
+            if (q1 >= 0 && q1 < g.len) v1 = __ldg(a.val + (size_t)(g.e0 + q1) * a.Kp + k);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(v0, v1);
+            w[e >> 1] = *reinterpret_cast<uint32_t*>(&p2);
+          }
+          *reinterpret_cast<uint4*>(sB + (n >> 3) * Cfg::kSBOB + gi * 128 + (n & 7) * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&fullB[s]);
+      }
+      if (*abort_flag) break;
+    }
+    // ------------------------------------------------ epilogue (warps 4-7) --
+    if (warp >= 4) {
+      const int q = warp & 3;
+      bool fin = mbar_wait(done, 0, kWaitLimit);
+      fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
+      if (!fin) {
+        if (lane == 0) tc_flag(kStatusTcTimeout);
+      } else {
+        tc_fence_after();
+        const int bc = bc0 + q * 32 + lane;
+        for (int j = 0; j < NT; ++j) {
+          const int wo = wc + j * kTW;
+          for (int k = 0; k < K; ++k) {
+            float v[16];
+            if (items > 0) {
+              tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + j * N + k * 16, v);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = 0.f;
+            }
+            if (bc < a.BC && wo < a.Wout) {
+              __nv_bfloat16* dst = a.X + (((size_t)bc * K + k) * a.Hout + ho) * a.Wout + wo;
+              const int n = min(16, a.Wout - wo);
+              if (n == 16) {
+                uint32_t w32[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+                  w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+                }
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
+              } else {
+                for (int e = 0; e < n; ++e) dst[e] = __float2bfloat16_rn(v[e]);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int K, int S>
+int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
+  using Cfg = TcCfg<K, S>;
+  auto enc = encode_fn();
+  if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int Hin = psi->grid_in.nlat, Win = psi->grid_in.nlon;
+  CUtensorMap map;
+  cuuint64_t dims[3] = {(cuuint64_t)Win, (cuuint64_t)Hin, (cuuint64_t)BC};
+  cuuint64_t strides[2] = {(cuuint64_t)Win * 2, (cuuint64_t)Hin * Win * 2};
+  cuuint32_t box[3] = {8, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  TcArgs a;
+  a.X = (__nv_bfloat16*)X;
+  a.val = psi->val;
+  a.runs = psi->runs;
+  a.run_ptr = psi->run_ptr;
+  a.row_order = psi->row_order;
+  a.BC = BC;
+  a.Hout = psi->grid_out.nlat;
+  a.Wout = psi->grid_out.nlon;
+  a.Win = Win;
+  a.Kp = psi->K_pad;
+  auto kern = fwd_tc_kernel<K, S>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) !=
+      cudaSuccess)
+    return check_launch("disco_fwd (tensor cores) attribute");
+  dim3 grid((a.Wout + kTW * Cfg::NT - 1) / (kTW * Cfg::NT), (BC + 127) / 128, a.Hout);
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(map, a);
+  return check_launch("disco_fwd (tensor cores)");
+}
+
+}  // namespace
+
+// Reads (and optionally clears) this unit's status word; the caller has
+// synchronised the device.
+cudaError_t tc_status(int32_t* v, bool clear) {
+  int32_t t = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&t, g_tc_status, sizeof(int32_t));
+  if (e == cudaSuccess && clear) {
+    const int32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof(int32_t));
+  }
+  *v |= t;
+  return e;
+}
+
+// Forward contraction on the tensor cores; returns DISCO_ERR_UNSUPPORTED
+// (without launching) for shapes this path does not take.
+int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
+  const int Win = psi->grid_in.nlon;
+  if (Win % 8 != 0 || (psi->s != 1 && psi->s != 2) || BC > 65535 * 128)
+    return DISCO_ERR_UNSUPPORTED;
+  const int K = psi->K;
+#define DISCO_TCASE(KK)                                                               \
+  if (K == KK) return psi->s == 1 ? launch_tc<KK, 1>(psi, x, X, BC, st)              \
+                                  : launch_tc<KK, 2>(psi, x, X, BC, st);
+  DISCO_TCASE(1)
+  DISCO_TCASE(2)
+  DISCO_TCASE(3)
+  DISCO_TCASE(4)
+  DISCO_TCASE(5)
+  DISCO_TCASE(6)
+  DISCO_TCASE(7)
+  DISCO_TCASE(8)
+  DISCO_TCASE(9)
+#undef DISCO_TCASE
+  return DISCO_ERR_UNSUPPORTED;
+}
+
+}  // namespace disco

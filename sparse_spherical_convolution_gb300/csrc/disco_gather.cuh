@@ -89,19 +89,22 @@ struct RowGather {
         const int offm = dc - 1;
         group_sync(bar_id, NT);
         {
-          const int nwin = single ? 1 : 2;
-          const int per = NCH * len_p;
-          const int total = per * nwin;
+          // one warp per window row (channel x side), lanes along the columns:
+          // coalesced loads, no integer division
+          const int nrows = NCH * (single ? 1 : 2);
           const int sp = imod(start_p, W), smn = imod(start_m, W);
-          for (int i = tid; i < total; i += NT) {
-            const int w2 = i >= per;
-            const int rem = i - w2 * per;
-            const int c = rem / len_p, j = rem - c * len_p;
-            const int col = ((w2 ? smn : sp) + j) % W;
+          for (int row = tid >> 5; row < nrows; row += NT / 32) {
+            const int w2 = row >= NCH;
+            const int c = row - w2 * NCH;
             const int bc = a.bc0 + c;
-            float v = 0.f;
-            if (bc < a.BC) v = to_f32(xrow[(size_t)bc * a.Hin * W + col]);
-            win[c * kPitch + w2 * len_p + j] = v;
+            const int base = w2 ? smn : sp;
+            float* dst = win + c * kPitch + w2 * len_p;
+            const T* src = xrow + (size_t)bc * a.Hin * W;
+            for (int j = tid & 31; j < len_p; j += 32) {
+              int col = base + j;
+              if (col >= W) col %= W;
+              dst[j] = (bc < a.BC) ? to_f32(src[col]) : 0.f;
+            }
           }
           for (int i = tid; i < dc * K; i += NT) {
             const int u = i / K, k = i - u * K;

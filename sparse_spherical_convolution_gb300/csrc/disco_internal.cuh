@@ -24,6 +24,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Validates the pieces of psi every hot call relies on.
 int check_psi(const disco_psi* psi);
 
+// Forward contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
+// without launching, for shapes that path does not take.
+int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st);
+
+// ORs the tensor-core unit's status word into *v (device already synchronised).
+cudaError_t tc_status(int32_t* v, bool clear);
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

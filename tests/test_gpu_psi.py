@@ -43,8 +43,20 @@ def test_psi_bit_exact(lib, case):
     assert np.array_equal(psi.tensor("csr_col").cpu().numpy(), ref.csr_col)
     val = psi.tensor("val").cpu().numpy()
     assert np.all(val[:, ref.K:] == 0)
-    assert ulp_diff_f32(val[:, :ref.K], ref.val.astype(np.float32)) <= 1
-    assert ulp_diff_f32(psi.tensor("csr_val").cpu().numpy(), ref.csr_val.astype(np.float32)) <= 1
+    _close_f32(val[:, :ref.K], ref.val)
+    _close_f32(psi.tensor("csr_val").cpu().numpy(), ref.csr_val)
+
+
+def _close_f32(gpu, ref64):
+    """Each value within 1 fp32 ulp of the fp64 oracle rounded to fp32, except
+    numerical zeros: a sin(bearing) that is 0 in exact arithmetic comes out as
+    +-1e-16-ish from either libm (e.g. sin(pi)), so values below 1e-9 of the
+    largest one are compared with that absolute floor instead."""
+    ref32 = ref64.astype(np.float32)
+    floor = 1e-9 * np.abs(ref64).max()
+    small = np.abs(ref64) < floor
+    assert np.all(np.abs(gpu[small].astype(np.float64) - ref64[small]) <= floor)
+    assert ulp_diff_f32(gpu[~small], ref32[~small]) <= 1
 
 
 @pytest.mark.parametrize("case", CASES[:2] + CASES[5:], ids=lambda c: f"{c[0]}->{c[1]}")
