@@ -203,6 +203,30 @@ DISCO_API int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, c
                                disco_dtype dtype, void* workspace, size_t workspace_bytes,
                                void* stream);
 
+/* Size of the fixed device scratch of disco_fused_conv_bwd_input_noalloc. */
+#define DISCO_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
+
+/* Allocation-free form of disco_fused_conv_bwd_input (the pages have no
+   counterpart; it exists for callers that cannot allocate device memory
+   themselves, e.g. a runtime whose allocator owns all device memory from
+   start-up, or a hot loop that must not risk the implicit device
+   synchronisation of cudaMalloc).  Same arguments, result and accuracy as
+   disco_fused_conv_bwd_input, without the workspace: the dX intermediate
+   lives in a fixed 64 MiB (DISCO_NOALLOC_SCRATCH_BYTES) device array that
+   every GPU loading this library holds until the process exits.  Problems
+   whose dX (B * Cin * K * H_out * W_out * 2 bytes) exceeds it are rejected
+   with DISCO_ERR_WORKSPACE before any launch.  The call allocates and frees
+   nothing.  The first call on a device looks up the array's device address
+   (cudaGetSymbolAddress, with that device current) and caches it; make that
+   first call before any stream capture.  All calls share the one array and
+   it keeps the last call's contents (dX is fully rewritten each call), so
+   calls that overlap on the GPU, e.g. on two streams, race and must be
+   serialised by the caller. */
+DISCO_API int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const void* dy,
+                                                 const void* W, void* gx, int32_t B,
+                                                 int32_t Cin, int32_t Cout, disco_dtype dtype,
+                                                 void* stream);
+
 /* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,

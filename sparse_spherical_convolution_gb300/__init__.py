@@ -20,8 +20,11 @@ __all__ = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
     "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
-    "disco_device_status", "library_path", "load_library", "EXPORTED_SYMBOLS",
+    "disco_fused_conv_bwd_input_noalloc", "disco_device_status", "library_path",
+    "load_library", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 DISCO_F32, DISCO_BF16 = 0, 1
 
@@ -29,7 +32,7 @@ EXPORTED_SYMBOLS = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
     "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
-    "disco_device_status",
+    "disco_fused_conv_bwd_input_noalloc", "disco_device_status",
 ]
 
 
@@ -102,6 +105,8 @@ def load_library():
     lib.disco_fused_conv_bwd_input_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
     lib.disco_fused_conv_bwd_input.restype = ctypes.c_int
     lib.disco_fused_conv_bwd_input.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
+    lib.disco_fused_conv_bwd_input_noalloc.restype = ctypes.c_int
+    lib.disco_fused_conv_bwd_input_noalloc.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P]
     lib.disco_device_status.restype = ctypes.c_int
     lib.disco_device_status.argtypes = [ctypes.POINTER(I32), I32]
     _lib = lib
@@ -207,6 +212,14 @@ def disco_fused_conv_bwd_input(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout
         ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy),
         _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
         _stream(stream)))
+
+
+def disco_fused_conv_bwd_input_noalloc(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout: int,
+                                       stream=None) -> None:
+    """disco_fused_conv_bwd_input without a workspace argument: the library's
+    fixed device scratch holds dX (see include/disco.h for limits and rules)."""
+    _check(load_library().disco_fused_conv_bwd_input_noalloc(
+        ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy), _stream(stream)))
 
 
 def disco_device_status(clear: bool = True) -> int:

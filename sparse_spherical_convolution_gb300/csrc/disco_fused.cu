@@ -30,6 +30,8 @@
 // in a device status word (read by disco_device_status), stops issuing work,
 // waits (bounded) for MMAs in flight and frees its TMEM before returning.
 
+#include <mutex>
+
 #include "disco_gather.cuh"
 #include "disco_umma.cuh"
 
@@ -526,4 +528,66 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
   if (e == cudaSuccess) e = tc_status(flags, clear != 0);
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
   return DISCO_OK;
+}
+
+// ------------------------------------------------ allocation-free variant --
+//
+// disco_fused_conv_bwd_input_noalloc: the same computation as
+// disco_fused_conv_bwd_input, for callers that cannot allocate device memory
+// themselves (for example a host runtime whose allocator owns all device
+// memory from start-up, or a hot loop that must not risk the implicit device
+// synchronisation cudaMalloc can cause).  Its dX scratch is the fixed array
+// below, which the CUDA runtime creates on every device that loads this
+// library and keeps until the process exits.  Host code cannot use the
+// array's name as a device address, so the address is looked up once per
+// device with cudaGetSymbolAddress (on the first call on that device, with
+// that device current) and cached.
+
+namespace disco {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = DISCO_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DISCO_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(DISCO_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DISCO_OK;
+}
+
+}  // namespace
+}  // namespace disco
+
+extern "C" int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const void* dy, const void* W,
+                                                  void* gx, int32_t B, int32_t Cin, int32_t Cout,
+                                                  disco_dtype dtype, void* stream) {
+  int st = check_fused_common(psi, dy, W, gx, B, Cin, Cout, dtype);
+  if (st) return st;
+  const size_t need = disco_fused_conv_bwd_input_workspace_bytes(psi, B, Cin, dtype);
+  if (need > kNoAllocScratchBytes)
+    return fail(DISCO_ERR_WORKSPACE,
+                "disco_fused_conv_bwd_input_noalloc: this problem needs %zu bytes of scratch, "
+                "the fixed scratch holds %zu (use disco_fused_conv_bwd_input with a workspace)",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch))) return st;
+  // dX is fully rewritten by the GEMM before the transpose reads it, so
+  // nothing left in the scratch by an earlier call needs clearing.
+  return disco_fused_conv_bwd_input(psi, dy, W, gx, B, Cin, Cout, dtype, scratch,
+                                    kNoAllocScratchBytes, stream);
 }
