@@ -105,6 +105,8 @@ typedef struct {
   int64_t nnz_csr;  /* CSR non-zeros summed over (k, ho) rows */
   int64_t nruns;    /* (ho, hi) segments */
   int64_t nhval;    /* rows of hval */
+  int64_t nftab;    /* elements of ftab */
+  int64_t nbtab;    /* elements of btab */
   size_t bytes;     /* device bytes disco_build_psi_kpacked needs */
   /* Union ("kpacked") layout, shared across k (§kpacked layout):
      neighbours of output row ho (for output longitude 0) are entries
@@ -125,6 +127,18 @@ typedef struct {
   int32_t* truns;       /* [nruns]: run indices ordered by (hi, ho) */
   float* hval;          /* [nhval][K_pad]: pair weights, see disco_run */
   int32_t* row_order;   /* [Hout]: output rows by descending work (launch order) */
+  /* bf16 tables of each run for the tensor-core tiles (values rounded from val).
+     Forward table of run r: K rows of TLf = roundup8(len + 16) elements at
+     ftab + ftab_off[r]; row k holds psi_k(delta) at index 8 + delta - dlo for
+     the run's offsets dlo..dhi and zeros elsewhere.
+     Transpose (polyphase) table of run r: K*s rows of TLb = roundup8(EH - EL + 17)
+     elements at btab + btab_off[r], EH = floor(dhi/s), EL = ceil((dlo - s + 1)/s);
+     row k*s + p holds psi_k(s*e + p) at index 8 + EH - e (offsets descending)
+     and zeros elsewhere. */
+  int32_t* ftab_off;    /* [nruns + 1], multiples of 8 */
+  uint16_t* ftab;       /* [nftab] */
+  int32_t* btab_off;    /* [nruns + 1], multiples of 8 */
+  uint16_t* btab;       /* [nbtab] */
 } disco_psi;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -172,7 +186,10 @@ DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B,
      gx[b,c,hi,wi] = sum_{k,ho,wo} sum_{wi0: (wi0 + wo*s) mod W_in = wi}
                        psi[k,ho,hi,wi0] * G[b,c,k,ho,wo]
    G: [B, C, K, H_out, W_out], gx: [B, C, H_in, W_in], both `dtype`.
-   Each thread block owns whole input rows (latitude-row ownership). */
+   Each thread block owns whole input rows (latitude-row ownership).  bf16
+   with W_in and W_out multiples of 8 runs on the tensor cores (polyphase
+   Toeplitz tiles, 4 input rows per block sharing each G window); other cases
+   run the CUDA-core gather. */
 DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
@@ -230,7 +247,8 @@ DISCO_API int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const voi
 /* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,
-   bit 2 = one of the tensor-core forward contraction timed out; a
+   bit 2 = one of the tensor-core forward contraction timed out,
+   bit 3 = one of the tensor-core transpose contraction timed out; a
    kernel that times out stops issuing work, frees its tensor memory and
    returns, leaving its outputs incomplete).  clear != 0 resets the word. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);

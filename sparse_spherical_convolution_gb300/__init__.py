@@ -55,14 +55,15 @@ class disco_run(ctypes.Structure):
 
 
 _PSI_ARRAYS = ["row_ptr", "idx", "val", "csr_row_ptr", "csr_col", "csr_val", "run_ptr", "runs",
-               "trun_ptr", "truns", "hval", "row_order"]
+               "trun_ptr", "truns", "hval", "row_order", "ftab_off", "ftab", "btab_off", "btab"]
 
 
 class disco_psi(ctypes.Structure):
     _fields_ = [("grid_in", disco_grid), ("grid_out", disco_grid), ("basis", disco_basis),
                 ("K", ctypes.c_int32), ("K_pad", ctypes.c_int32), ("s", ctypes.c_int32),
                 ("max_row", ctypes.c_int32), ("nnz", ctypes.c_int64), ("nnz_csr", ctypes.c_int64),
-                ("nruns", ctypes.c_int64), ("nhval", ctypes.c_int64), ("bytes", ctypes.c_size_t)] + \
+                ("nruns", ctypes.c_int64), ("nhval", ctypes.c_int64), ("nftab", ctypes.c_int64),
+                ("nbtab", ctypes.c_int64), ("bytes", ctypes.c_size_t)] + \
                [(n, ctypes.c_void_p) for n in _PSI_ARRAYS]
 
 
@@ -239,7 +240,8 @@ class Psi:
 
     _DT = {"row_ptr": "int32", "idx": "int32", "val": "float32", "csr_row_ptr": "int32",
            "csr_col": "int32", "csr_val": "float32", "run_ptr": "int32", "runs": "int32",
-           "trun_ptr": "int32", "truns": "int32", "hval": "float32", "row_order": "int32"}
+           "trun_ptr": "int32", "truns": "int32", "hval": "float32", "row_order": "int32",
+           "ftab_off": "int32", "ftab": "int16", "btab_off": "int32", "btab": "int16"}
 
     def __init__(self, grid_in, grid_out, kind: int, n_radial: int, cutoff: float, stream=None):
         import torch
@@ -258,7 +260,8 @@ class Psi:
                 "csr_row_ptr": (c.K * Hout + 1,), "csr_col": (c.nnz_csr,),
                 "csr_val": (c.nnz_csr,), "run_ptr": (Hout + 1,), "runs": (c.nruns, 8),
                 "trun_ptr": (Hin + 1,), "truns": (c.nruns,), "hval": (c.nhval, c.K_pad),
-                "row_order": (Hout,)}
+                "row_order": (Hout,), "ftab_off": (c.nruns + 1,), "ftab": (c.nftab,),
+                "btab_off": (c.nruns + 1,), "btab": (c.nbtab,)}
 
     def tensor(self, name: str):
         """Device view of one psi array (for inspection and tests)."""

@@ -41,6 +41,7 @@ struct ContractArgs {
   const int32_t* trun_ptr;
   const int32_t* truns;
   const float* hval;
+  const float* hval_full;  // union layout values [nnz][Kp] (signed offsets)
   const int32_t* row_order;
   int vec_ok;  // output rows are 16-byte aligned
 };
@@ -124,93 +125,129 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const ContractArgs a) 
 
 // ----------------------------------------------------------- transpose --
 //
-// gx[bc,hi,wi] = sum_{runs reading hi} sum_k sum_{delta=0..D} w_k(delta) *
-//                (G_k[ho, (wi - delta)/S] +/- G_k[ho, (wi + delta)/S])
-// (terms only where S divides wi -/+ delta).  One block owns 32 channels x
-// 64 columns of input row hi; the runs that read hi come from psi.truns.
-template <int S>
-struct TWin {
-  static constexpr int kSingle = (kTile - 1 + 2 * kDCMax) / S + 1;
-  static constexpr int kDouble = (kTile - 1 + kDCMax) / S + 1;
-  static constexpr int kLen = (kSingle > 2 * kDouble) ? kSingle : 2 * kDouble;
+// gx[bc,hi,j] = sum_{runs (ho, hi)} sum_k sum_{delta in run} psi_k(delta) * G_k[ho, (j - delta)/S]
+// (terms only where S divides j - delta).  Polyphase form: with j = S q + p
+// and delta = S e + p, gx[S q + p] = sum psi_k(S e + p) G_k[q - e], i.e. a
+// correlation per phase p on the decimated index q.
+//
+// One block owns input row hi, 32 channels (one per lane) and 64 decimated
+// positions (S * 64 input columns); a thread owns 8 positions x S phases.
+// Per run and chunk of up to kBDC offsets the block stages the G windows of
+// ALL K planes (bf16, pitch = 2 mod 4 elements so the 32 lanes hit 32 banks)
+// and the run's psi values for the chunk, then every thread accumulates
+// K x (offsets) x 8 terms per phase in registers.  For S = 2 both phases
+// read the same 11 staged values per block of 8 offsets.
+constexpr int kBQ = 64;     // decimated positions per block
+constexpr int kBT = 8;      // decimated positions per thread
+constexpr int kBDC = 32;    // offsets per staged chunk (multiple of 8)
+
+// staged G window element: bf16 bits for bf16 inputs (exact), fp32 for fp32
+template <typename T>
+struct BwdStage {
+  using E = uint16_t;
+  __device__ static E put(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+  __device__ static float get(E e) { return __uint_as_float((uint32_t)e << 16); }
 };
+template <>
+struct BwdStage<float> {
+  using E = float;
+  __device__ static E put(float v) { return v; }
+  __device__ static float get(E e) { return e; }
+};
+
+template <typename T, int S>
+struct BwdWin {
+  static constexpr int kLen = kBQ + kBDC / S + 2;  // G window per k and channel
+  // row pitch in elements: 32 lanes (channels) must hit 32 different banks
+  static constexpr int kPitch = sizeof(typename BwdStage<T>::E) == 2 ? ((kLen + 1) / 4) * 4 + 2
+                                                                      : (kLen | 1);
+};
+
+template <typename T, int K, int S>
+constexpr size_t bwd_smem() {
+  return (size_t)K * 32 * BwdWin<T, S>::kPitch * sizeof(typename BwdStage<T>::E) +
+         (size_t)K * kBDC * sizeof(float);
+}
 
 template <typename T, int K, int S, bool ANISO>
 __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) {
-  extern __shared__ float sm[];
-  constexpr int kPitch = TWin<S>::kLen | 1;
-  float* win = sm;
-  float* wts = sm + 32 * kPitch;
+  extern __shared__ __align__(16) uint8_t bsm[];
+  using St = BwdStage<T>;
+  using E = typename St::E;
+  constexpr int kPitch = BwdWin<T, S>::kPitch;
+  E* sG = reinterpret_cast<E*>(bsm);                                            // [K][32][kPitch]
+  float* sW = reinterpret_cast<float*>(bsm + (size_t)K * 32 * kPitch * sizeof(E));  // [K][kBDC]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hi = blockIdx.z;
   const int bc0 = blockIdx.y * 32;
-  const int wi_blk = blockIdx.x * kTile;  // multiple of S
-  const int o0 = warp * kTW;              // multiple of S
+  const int qb = blockIdx.x * kBQ;
+  const int q0 = warp * kBT;  // first decimated position of this thread inside the block
   const T* G = reinterpret_cast<const T*>(a.in);
   const int Wo = a.Wout;
+  const size_t plane = (size_t)K * a.Hout * Wo;
 
-  float acc[kTW];
+  float acc[S][kBT];
 #pragma unroll
-  for (int t = 0; t < kTW; ++t) acc[t] = 0.f;
+  for (int p = 0; p < S; ++p)
+#pragma unroll
+    for (int t = 0; t < kBT; ++t) acc[p][t] = 0.f;
 
   const int t_begin = a.trun_ptr[hi], t_end = a.trun_ptr[hi + 1];
   for (int tr = t_begin; tr < t_end; ++tr) {
     const disco_run run = a.runs[a.truns[tr]];
-    const int steps = run.D + 1;
-    const int dc = min(kDCMax, (steps + 7) & ~7);
-    for (int k = 0; k < K; ++k) {
-      const T* Gk = G + ((size_t)k * a.Hout + run.ho) * Wo;
-      const size_t plane = (size_t)K * a.Hout * Wo;
-      for (int da = 0; da < steps; da += dc) {
-        const int nd = min(dc, steps - da);
-        const bool single = (da == 0);
-        // minus side: wo = (wi - delta)/S = start_m + (o - u + offm)/S
-        // plus side:  wo = (wi + delta)/S = start_p + (o + u + offp)/S
-        const int len_p = single ? (kTile - 1 + 2 * dc) / S + 1 : (kTile - 1 + dc) / S + 1;
-        const int start_m = (wi_blk - da - dc) / S;  // exact: all terms multiples of S
-        const int start_p = single ? start_m : (wi_blk + da) / S;
-        const int offm = dc;
-        const int offp = single ? dc : 0;
-        float* wm = win;
-        float* wp = single ? win : win + len_p;
-        __syncthreads();
-        {
-          // one warp per window row (channel x side), lanes along the columns
-          const int nrows = 32 * (single ? 1 : 2);
-          const int smn = imod(start_m, Wo), sp = imod(start_p, Wo);
-          for (int row = threadIdx.x >> 5; row < nrows; row += kThreads / 32) {
-            const int w2 = row >= 32;
-            const int c = row - w2 * 32;
-            const int bc = bc0 + c;
-            const int base = w2 ? sp : smn;
-            float* dst = win + c * kPitch + w2 * len_p;
-            const T* src = Gk + bc * plane;
-            for (int j = lane; j < len_p; j += 32) {
-              int col = base + j;
-              if (col >= Wo) col %= Wo;
-              dst[j] = (bc < a.BC) ? ld_in(src + col) : 0.f;
-            }
-          }
-          for (int i = threadIdx.x; i < dc; i += kThreads)
-            wts[i] = (i < nd) ? a.hval[(size_t)(run.hoff + da + i) * a.Kp + k] : 0.f;
+    const int dlo = (run.len == a.Win) ? -(a.Win / 2) : -run.npair;
+    const int dhi = dlo + run.len - 1;
+    const int dstart = (dlo >= 0) ? (dlo & ~7) : -(((-dlo) + 7) & ~7);  // multiple of 8, <= dlo
+    for (int da = dstart; da <= dhi; da += kBDC) {
+      // decimated G index of (j, delta) is (j - delta)/S; over the block and chunk
+      // it runs from gs = (S*qb - da - kBDC)/S upward (exact: all multiples of S)
+      const int gs = (S * qb - da - kBDC) / S;
+      __syncthreads();
+      // stage G windows of all K planes: one warp per (k, channel) row
+      const int g0 = imod(gs, Wo);
+      for (int row = warp; row < K * 32; row += kThreads / 32) {
+        const int k = row >> 5, c = row & 31;
+        const int bc = bc0 + c;
+        const T* src = G + (size_t)bc * plane + ((size_t)k * a.Hout + run.ho) * Wo;
+        E* dst = sG + (size_t)row * kPitch;
+        for (int i = lane; i < BwdWin<T, S>::kLen; i += 32) {
+          int col = g0 + i;
+          if (col >= Wo) col %= Wo;
+          dst[i] = St::put((bc < a.BC) ? to_f32(src[col]) : 0.f);
         }
-        __syncthreads();
-        const bool neg = ANISO && (k % 3 == 2);
-        for (int ub = 0; ub < nd; ub += 8) {
-          // o0, ub, offm, offp are multiples of S, so both bases are exact and
-          // the per-(t, u) offsets below are compile-time constants
-          const float* bm = wm + lane * kPitch + (o0 - ub + offm) / S;
-          const float* bp = wp + lane * kPitch + (o0 + ub + offp) / S;
+      }
+      // psi values of the chunk, signed offsets, zero outside the run
+      for (int i = threadIdx.x; i < K * kBDC; i += kThreads) {
+        const int k = i / kBDC, u = i - k * kBDC;
+        const int d = da + u;
+        sW[i] = (d >= dlo && d <= dhi) ? a.hval_full[(size_t)(run.e0 + d - dlo) * a.Kp + k] : 0.f;
+      }
+      __syncthreads();
+      const int nub = min(kBDC, dhi - da + 1);
+#pragma unroll 1
+      for (int k = 0; k < K; ++k) {
+        const E* gk = sG + ((size_t)k * 32 + lane) * kPitch;
+        const float* wk = sW + k * kBDC;
+        for (int ub = 0; ub < nub; ub += 8) {
+          // window index of (position qb + q0 + t, delta = da + ub + u, phase p):
+          //   qb + q0 + t - (da + ub)/S + (p - u)/S - gs,  and qb - gs = (da + kBDC)/S,
+          //   so it is base + t + (p - u)/S with base = q0 + (kBDC - ub)/S,
+          //   which stays in [1, kBQ - 1 + kBDC/S] < the staged window length
+          const int base = q0 + (kBDC - ub) / S;
+          float w[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) w[u] = wk[ub + u];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float w = wts[ub + u];
 #pragma unroll
-            for (int t = 0; t < kTW; ++t) {
-              if ((t - u) % S != 0) continue;  // S must divide wi -/+ delta
-              const float gm = bm[(t - u) / S];
-              const float gp = bp[(t + u) / S];
-              acc[t] = fmaf(w, neg ? gm - gp : gm + gp, acc[t]);
+            for (int p = 0; p < S; ++p) {
+              if (((p - u) % S + S) % S != 0) continue;
+#pragma unroll
+              for (int t = 0; t < kBT; ++t) {
+                const float gv = St::get(gk[base + t + (p - u) / S]);
+                acc[p][t] = fmaf(w[u], gv, acc[p][t]);
+              }
             }
           }
         }
@@ -219,20 +256,27 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) 
   }
 
   const int bc = bc0 + lane;
-  const int wi = wi_blk + o0;
-  if (bc >= a.BC || wi >= a.Win) return;
-  const int n = min(kTW, a.Win - wi);
+  if (bc >= a.BC) return;
   T* gx = reinterpret_cast<T*>(a.out);
-  store8<T>(gx + ((size_t)bc * a.Hin + hi) * a.Win + wi, acc, n, a.vec_ok != 0);
+  T* row = gx + ((size_t)bc * a.Hin + hi) * a.Win;
+  // output columns j = S*(qb + q0 + t) + p
+  float v[S * kBT];
+#pragma unroll
+  for (int t = 0; t < kBT; ++t)
+#pragma unroll
+    for (int p = 0; p < S; ++p) v[t * S + p] = acc[p][t];
+  const int j0 = S * (qb + q0);
+  if (j0 >= a.Win) return;
+#pragma unroll
+  for (int h = 0; h < S; ++h) {
+    const int jj = j0 + h * 8;
+    if (jj < a.Win) store8<T>(row + jj, v + h * 8, min(8, a.Win - jj), a.vec_ok != 0);
+  }
 }
 
 template <typename T, int K, int S, bool ANISO>
 constexpr size_t fwd_smem() {
   return (size_t)FwdGather<T, K, S, ANISO>::kSmemFloats * sizeof(float);
-}
-template <int S>
-constexpr size_t bwd_smem() {
-  return (size_t)(32 * (TWin<S>::kLen | 1) + kDCMax) * sizeof(float);
 }
 
 template <typename T, int K, int S, bool ANISO>
@@ -250,11 +294,11 @@ int launch_fwd(const ContractArgs& a, cudaStream_t st) {
 template <typename T, int K, int S, bool ANISO>
 int launch_bwd(const ContractArgs& a, cudaStream_t st) {
   auto kern = bwd_kernel<T, K, S, ANISO>;
-  size_t smem = bwd_smem<S>();
+  size_t smem = bwd_smem<T, K, S>();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return check_launch("disco_bwd attribute");
-  dim3 grid((a.Win + kTile - 1) / kTile, (a.BC + 31) / 32, a.Hin);
+  dim3 grid((a.Win + S * kBQ - 1) / (S * kBQ), (a.BC + 31) / 32, a.Hin);
   kern<<<grid, kThreads, smem, st>>>(a);
   return check_launch("disco_bwd");
 }
@@ -305,14 +349,15 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   a.trun_ptr = psi->trun_ptr;
   a.truns = psi->truns;
   a.hval = psi->hval;
+  a.hval_full = psi->val;
   a.row_order = psi->row_order;
   int elems16 = dtype == DISCO_F32 ? 4 : 8;
   a.vec_ok = ((fwd ? a.Wout : a.Win) % elems16) == 0;
   cudaStream_t s = (cudaStream_t)stream;
   int kind = psi->basis.kind, K = psi->K;
-  if (fwd && dtype == DISCO_BF16) {
-    // bf16 forward: the tensor-core Toeplitz kernel where its shape rules hold
-    const int tst = fwd_tensor_core(psi, in, out, a.BC, s);
+  if (dtype == DISCO_BF16) {
+    // bf16: the tensor-core Toeplitz kernels where their shape rules hold
+    const int tst = fwd ? fwd_tensor_core(psi, in, out, a.BC, s) : bwd_tensor_core(psi, in, out, a.BC, s);
     if (tst != DISCO_ERR_UNSUPPORTED) return tst;
   }
   if (dtype == DISCO_F32)

@@ -316,8 +316,9 @@ __global__ void __launch_bounds__(kGThreads, 2) dx_gemm_kernel(const GemmArgs a)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kGStage);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t p0 = (int64_t)blockIdx.x * kGM;
-  const int n0 = blockIdx.y * kGN;
+  // C*K tiles vary fastest so consecutive CTAs reuse one dy tile from L2
+  const int64_t p0 = (int64_t)blockIdx.y * kGM;
+  const int n0 = blockIdx.x * kGN;
   const int b = blockIdx.z;
   const int nk = (a.Cout + kGK - 1) / kGK;
   const __nv_bfloat16* dyb = a.dy + (size_t)b * a.Cout * a.P;
@@ -336,7 +337,6 @@ __global__ void __launch_bounds__(kGThreads, 2) dx_gemm_kernel(const GemmArgs a)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   bool ok = true;
-  const bool vec_p = (a.P % 8) == 0;
 
   for (int kc = 0; kc < nk; ++kc) {
     const int s = kc & 1;
@@ -353,37 +353,47 @@ __global__ void __launch_bounds__(kGThreads, 2) dx_gemm_kernel(const GemmArgs a)
       break;
     }
     const int o_base = kc * kGK;
-    // A: dy[o][p0 .. p0+127] -> (row p, k o); 8 pixels per 16-byte load
-    for (int i = tid; i < kGK * (kGM / 8); i += kGThreads) {
-      const int ol = i / (kGM / 8), pg = i - ol * (kGM / 8);
-      const int o = o_base + ol;
-      const int64_t p = p0 + pg * 8;
-      __align__(16) __nv_bfloat16 v[8];
-      if (o < a.Cout && vec_p && p + 8 <= a.P) {
-        *reinterpret_cast<uint4*>(v) = *reinterpret_cast<const uint4*>(dyb + (size_t)o * a.P + p);
-      } else {
-        for (int e = 0; e < 8; ++e)
-          v[e] = (o < a.Cout && p + e < a.P) ? dyb[(size_t)o * a.P + p + e] : __float2bfloat16_rn(0.f);
-      }
+    // A: (row p, k o) <- dy[o][p].  A thread gathers 8 consecutive o of one
+    // pixel (lanes on consecutive pixels: coalesced 2-byte loads) and writes
+    // them as one 16-byte core-matrix row.
+    for (int i = tid; i < kGM * (kGK / 8); i += kGThreads) {
+      const int pl = i % kGM, og = i / kGM;
+      const int64_t p = p0 + pl;
+      uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        *reinterpret_cast<__nv_bfloat16*>(sA + kmajor_off(pg * 8 + e, ol, kGSBO)) = v[e];
+      for (int e = 0; e < 8; e += 2) {
+        const int o = o_base + og * 8 + e;
+        __nv_bfloat16 v0 = __float2bfloat16_rn(0.f), v1 = v0;
+        if (p < a.P) {
+          if (o < a.Cout) v0 = dyb[(size_t)o * a.P + p];
+          if (o + 1 < a.Cout) v1 = dyb[(size_t)(o + 1) * a.P + p];
+        }
+        __nv_bfloat162 p2;
+        p2.x = v0;
+        p2.y = v1;
+        w[e >> 1] = *reinterpret_cast<uint32_t*>(&p2);
+      }
+      *reinterpret_cast<uint4*>(sA + kmajor_off(pl, og * 8, kGSBO)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    // B: W[o][n0 .. n0+127] -> (row n, k o)
-    for (int i = tid; i < kGK * (kGN / 8); i += kGThreads) {
-      const int ol = i / (kGN / 8), ng = i - ol * (kGN / 8);
-      const int o = o_base + ol;
-      const int n = n0 + ng * 8;
-      __align__(16) __nv_bfloat16 v[8];
-      if (o < a.Cout && n + 8 <= a.CK && (a.CK % 8) == 0) {
-        *reinterpret_cast<uint4*>(v) = *reinterpret_cast<const uint4*>(a.W + (size_t)o * a.CK + n);
-      } else {
-        for (int e = 0; e < 8; ++e)
-          v[e] = (o < a.Cout && n + e < a.CK) ? a.W[(size_t)o * a.CK + n + e] : __float2bfloat16_rn(0.f);
-      }
+    // B: (row n, k o) <- W[o][n], same scheme along n
+    for (int i = tid; i < kGN * (kGK / 8); i += kGThreads) {
+      const int nl = i % kGN, og = i / kGN;
+      const int n = n0 + nl;
+      uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        *reinterpret_cast<__nv_bfloat16*>(sB + kmajor_off(ng * 8 + e, ol, kGSBO)) = v[e];
+      for (int e = 0; e < 8; e += 2) {
+        const int o = o_base + og * 8 + e;
+        __nv_bfloat16 v0 = __float2bfloat16_rn(0.f), v1 = v0;
+        if (n < a.CK) {
+          if (o < a.Cout) v0 = a.W[(size_t)o * a.CK + n];
+          if (o + 1 < a.Cout) v1 = a.W[(size_t)(o + 1) * a.CK + n];
+        }
+        __nv_bfloat162 p2;
+        p2.x = v0;
+        p2.y = v1;
+        w[e >> 1] = *reinterpret_cast<uint32_t*>(&p2);
+      }
+      *reinterpret_cast<uint4*>(sB + kmajor_off(nl, og * 8, kGSBO)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -508,8 +518,8 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   if (cudaFuncSetAttribute(dx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kGSmem) != cudaSuccess)
     return check_launch("dX gemm attribute");
-  dim3 grid((unsigned)((g.P + kGM - 1) / kGM), (g.CK + kGN - 1) / kGN, B);
-  if (grid.y > 65535) return fail(DISCO_ERR_UNSUPPORTED, "Cin*K too large");
+  dim3 grid((g.CK + kGN - 1) / kGN, (unsigned)((g.P + kGM - 1) / kGM), B);
+  if (grid.y > 65535) return fail(DISCO_ERR_UNSUPPORTED, "H_out * W_out too large");
   dx_gemm_kernel<<<grid, kGThreads, kGSmem, s>>>(g);
   if ((st = check_launch("dX gemm"))) return st;
   return disco_bwd(psi, workspace, gx, B, Cin, dtype, stream);
@@ -526,6 +536,7 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
     e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int32_t));
   }
   if (e == cudaSuccess) e = tc_status(flags, clear != 0);
+  if (e == cudaSuccess) e = btc_status(flags, clear != 0);
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
   return DISCO_OK;
 }

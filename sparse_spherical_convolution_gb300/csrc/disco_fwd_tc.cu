@@ -47,14 +47,25 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBuilderThreads = 192;   // warps 2..7
 constexpr int kTW = 16;                // output columns per MMA tile
-constexpr int kCK = 8;                 // K steps (16 window columns) per chunk
-constexpr int kChunkCols = kCK * 16;   // 128
-constexpr int kStages = 2;
+constexpr int kCK = 4;                 // K steps (16 window columns) per chunk
+constexpr int kChunkCols = kCK * 16;   // 64
 constexpr uint32_t kGroupBytes = 128 * 16;  // one TMA box: 128 rows x 8 bf16
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTcTimeout = 4;
 
 __device__ __forceinline__ void tc_flag(int bit) { atomicOr(&g_tc_status, bit); }
+
+// true in every thread of the named-barrier group iff `pred` holds in all of them
+__device__ __forceinline__ bool group_all_b(bool pred, int bar_id, int nthreads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(bar_id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ int wrap_col(int c, int W) {
   int r = c % W;
@@ -78,16 +89,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 
 struct TcArgs {
   __nv_bfloat16* X;   // [BC][K][Hout][Wout]
-  const float* val;   // union layout values [nnz][Kp]
   const disco_run* runs;
   const int32_t* run_ptr;
   const int32_t* row_order;
-  int BC, Hout, Wout, Win, Kp;
+  const int32_t* ftab_off;
+  const uint16_t* ftab;  // per run: K rows of TL = roundup8(len + 16), psi_k(delta) at 8 + delta - dlo
+  int BC, Hout, Wout, Win;
+  int TLB;            // table row capacity (>= every run's row length)
 };
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 // geometry of one run for the Toeplitz tiles
 struct RunGeom {
-  int hi, e0, dlo, len, M, KS;
+  int hi, e0, dlo, len, M, KS, TL;
 };
 
 template <int S>
@@ -100,36 +121,45 @@ __device__ __forceinline__ RunGeom run_geom(const disco_run& r, int Win) {
   g.M = ((-g.dlo) + 7) & ~7;
   const int L = S * (kTW - 1) + 2 * g.M + 1;
   g.KS = (L + 15) >> 4;
+  g.TL = (r.len + 16 + 7) & ~7;
   return g;
 }
 
-template <int K, int S>
+template <int K, int S, int STAGES>
 struct TcCfg {
-  static constexpr int N = 16 * K;                      // MMA N
-  static constexpr uint32_t kBBytes = N * kChunkCols * 2;  // B chunk
-  static constexpr uint32_t kSBOB = (kChunkCols / 8) * 128;  // 2048
-  static constexpr int NT = (512 / N) < 4 ? (512 / N) : 4;  // tiles per CTA
+  static constexpr int N = 16 * K;                           // MMA N
+  static constexpr uint32_t kBBytes = N * kChunkCols * 2;    // B chunk
+  static constexpr uint32_t kSBOB = (kChunkCols / 8) * 128;  // 1024
+  static constexpr int NT = (512 / N) < 4 ? (512 / N) : 4;   // tiles per CTA
   static constexpr int AG = (kChunkCols + S * kTW * (NT - 1)) / 8;  // A groups per stage
   static constexpr uint32_t kABytes = AG * kGroupBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = (NT * N <= 32) ? 32 : (NT * N <= 64) ? 64 : (NT * N <= 128) ? 128
                                         : (NT * N <= 256) ? 256 : 512;
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 128;
+  static constexpr size_t kFixed = (size_t)STAGES * kStageBytes + 256;
+  // two psi table buffers (double-buffered across runs): K rows x TLB bf16 each
+  __host__ __device__ static size_t tab_bytes(int TLB) { return ((size_t)K * TLB * 2 + 127) & ~(size_t)127; }
+  static size_t smem(int TLB) { return kFixed + 2 * tab_bytes(TLB); }
 };
 
-template <int K, int S>
+template <int K, int S, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
-  using Cfg = TcCfg<K, S>;
+  using Cfg = TcCfg<K, S, STAGES>;
   constexpr int N = Cfg::N, NT = Cfg::NT;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes);
-  uint64_t* fullA = bars;          // [2] TMA bytes landed
-  uint64_t* fullB = bars + 2;      // [2] B chunk built (192 arrivals)
-  uint64_t* empty = bars + 4;      // [2] MMAs of the stage done (commit)
-  uint64_t* done = bars + 6;       // all MMAs done (commit)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 7);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::kStageBytes);
+  uint64_t* fullA = bars;                 // [STAGES] TMA bytes landed
+  uint64_t* fullB = bars + STAGES;        // [STAGES] B chunk built (192 arrivals)
+  uint64_t* empty = bars + 2 * STAGES;    // [STAGES] MMAs of the stage done (commit)
+  uint64_t* done = bars + 3 * STAGES;     // all MMAs done (commit)
+  uint64_t* tfull = bars + 3 * STAGES + 1;   // [2] run table landed (bulk copy bytes)
+  uint64_t* tempty = bars + 3 * STAGES + 3;  // [2] run table released (192 builder arrivals)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 6);
+  // psi tables of two consecutive runs: [2][K][TLB] bf16
+  uint8_t* tabs = smem + Cfg::kFixed;
+  const size_t tab_bytes = Cfg::tab_bytes(a.TLB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ho = a.row_order[blockIdx.z];
@@ -138,12 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r_begin = a.run_ptr[ho], r_end = a.run_ptr[ho + 1];
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&fullA[s], 1);
       mbar_init(&fullB[s], kBuilderThreads);
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kBuilderThreads);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,9 +202,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = r_begin; r < r_end && !aborted; ++r) {
         const RunGeom g = run_geom<S>(a.runs[r], a.Win);
         const int u0 = S * wc - g.M;
+        {
+          // the run's psi table into buffer (run index & 1), once the builders released it
+          const int rl = r - r_begin, b = rl & 1;
+          if (rl >= 2 && !mbar_wait(&tempty[b], ((rl >> 1) - 1) & 1, kWaitLimit)) {
+            tc_flag(kStatusTcTimeout);
+            *abort_flag = 1;
+            aborted = true;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)K * g.TL * 2;
+          mbar_expect_tx(&tfull[b], bytes);
+          bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+        }
         for (int c = 0; c * kCK < g.KS; ++c, ++i) {
-          const int s = i & 1;
-          if ((i >= kStages && !mbar_wait(&empty[s], ((i >> 1) - 1) & 1, kWaitLimit)) || *abort_flag) {
+          const int s = i % STAGES;
+          if ((i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitLimit)) || *abort_flag) {
             tc_flag(kStatusTcTimeout);
             *abort_flag = 1;
             aborted = true;
@@ -188,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (aborted) {
         // let the copies this thread issued land (bounded) before the CTA exits
-        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
+        for (int back = 1; back <= STAGES && i - back >= 0; ++back) {
           const int li = i - back;
-          mbar_wait(&fullA[li & 1], (li >> 1) & 1, kWaitLimit);
+          mbar_wait(&fullA[li % STAGES], (li / STAGES) & 1, kWaitLimit);
         }
       }
     }
@@ -203,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = r_begin; r < r_end && ok; ++r) {
         const RunGeom g = run_geom<S>(a.runs[r], a.Win);
         for (int c = 0; c * kCK < g.KS; ++c, ++i) {
-          const int s = i & 1;
-          const uint32_t ph = (i >> 1) & 1;
+          const int s = i % STAGES;
+          const uint32_t ph = (i / STAGES) & 1;
           if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) ||
               *abort_flag) {
             tc_flag(kStatusTcTimeout);
@@ -233,33 +280,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------- B builders (6 warps) --
     const int btid = tid - 64;
     int i = 0;
-    for (int r = r_begin; r < r_end; ++r) {
+    bool ok = true;
+    for (int r = r_begin; r < r_end && ok; ++r) {
       const RunGeom g = run_geom<S>(a.runs[r], a.Win);
-      for (int c = 0; c * kCK < g.KS; ++c, ++i) {
-        const int s = i & 1;
-        bool ok = true;
-        if (i >= kStages) ok = mbar_wait(&empty[s], ((i >> 1) - 1) & 1, kWaitLimit);
-        if (!ok || *abort_flag) {
-          if (!ok) tc_flag(kStatusTcTimeout);
+      const int rl = r - r_begin, tb = rl & 1;
+      const uint16_t* tab = reinterpret_cast<const uint16_t*>(tabs + tb * tab_bytes);
+      {
+        bool mine = mbar_wait(&tfull[tb], (rl >> 1) & 1, kWaitLimit) && !*abort_flag;
+        if (!mine) {
+          tc_flag(kStatusTcTimeout);
           *abort_flag = 1;
-          break;
         }
+        ok = group_all_b(mine, 1, kBuilderThreads);
+        if (!ok) break;
+      }
+      for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+        const int s = i % STAGES;
+        bool mine = true;
+        if (i >= STAGES) mine = mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitLimit);
+        mine = mine && !*abort_flag;
+        if (!mine) {
+          tc_flag(kStatusTcTimeout);
+          *abort_flag = 1;
+        }
+        ok = group_all_b(mine, 1, kBuilderThreads);
+        if (!ok) break;
         uint8_t* sB = smem + s * Cfg::kStageBytes + Cfg::kABytes;
         const int nks = min(kCK, g.KS - c * kCK);
         const int ngrp = 2 * nks;  // 8-column groups of this chunk
         for (int idx = btid; idx < N * ngrp; idx += kBuilderThreads) {
           const int n = idx % N, gi = idx / N;
           const int k = n >> 4, t = n & 15;
-          const int d0 = c * kChunkCols + 8 * gi - S * t - g.M;  // offset delta of column 0 of the group
-          uint32_t w[4];
+          // table index of the first of the 8 consecutive offsets of this group
+          const int x0 = 8 + c * kChunkCols + 8 * gi - S * t - g.M - g.dlo;
+          uint32_t w[4] = {0u, 0u, 0u, 0u};
+          if (x0 + 7 >= 0 && x0 < g.TL) {
+            const uint16_t* row = tab + (size_t)k * g.TL;
+            uint16_t v[8];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            float v0 = 0.f, v1 = 0.f;
-            const int q0 = d0 + e - g.dlo, q1 = q0 + 1;
-            if (q0 >= 0 && q0 < g.len) v0 = __ldg(a.val + (size_t)(g.e0 + q0) * a.Kp + k);
-            if (q1 >= 0 && q1 < g.len) v1 = __ldg(a.val + (size_t)(g.e0 + q1) * a.Kp + k);
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(v0, v1);
-            w[e >> 1] = *reinterpret_cast<uint32_t*>(&p2);
+            for (int e = 0; e < 8; ++e) {
+              const int x = x0 + e;
+              v[e] = (x >= 0 && x < g.TL) ? row[x] : (uint16_t)0;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = (uint32_t)v[2 * e] | ((uint32_t)v[2 * e + 1] << 16);
           }
           *reinterpret_cast<uint4*>(sB + (n >> 3) * Cfg::kSBOB + gi * 128 + (n & 7) * 16) =
               make_uint4(w[0], w[1], w[2], w[3]);
@@ -267,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&fullB[s]);
       }
-      if (*abort_flag) break;
+      if (ok) mbar_arrive(&tempty[tb]);  // this run's table is no longer read
     }
     // ------------------------------------------------ epilogue (warps 4-7) --
     if (warp >= 4) {
@@ -331,12 +395,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+template <int K, int S, int STAGES>
+int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, TcArgs a, cudaStream_t st) {
+  using Cfg = TcCfg<K, S, STAGES>;
+  const size_t smem = Cfg::smem(a.TLB);
+  auto kern = fwd_tc_kernel<K, S, STAGES>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return check_launch("disco_fwd (tensor cores) attribute");
+  dim3 grid((a.Wout + kTW * Cfg::NT - 1) / (kTW * Cfg::NT), (a.BC + 127) / 128, a.Hout);
+  kern<<<grid, kThreads, smem, st>>>(map, a);
+  return check_launch("disco_fwd (tensor cores)");
+}
+
 template <int K, int S>
 int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
-  using Cfg = TcCfg<K, S>;
+  constexpr size_t kMaxSmem = 227 * 1024;
+  const int Hin = psi->grid_in.nlat, Win = psi->grid_in.nlon;
+  TcArgs a;
+  a.X = (__nv_bfloat16*)X;
+  a.runs = psi->runs;
+  a.run_ptr = psi->run_ptr;
+  a.row_order = psi->row_order;
+  a.ftab_off = psi->ftab_off;
+  a.ftab = psi->ftab;
+  a.BC = BC;
+  a.Hout = psi->grid_out.nlat;
+  a.Wout = psi->grid_out.nlon;
+  a.Win = Win;
+  a.TLB = (Win + 16 + 7) & ~7;  // a run is at most one ring long
+  if (!psi->ftab || !psi->ftab_off) return DISCO_ERR_UNSUPPORTED;
+  const bool fit3 = TcCfg<K, S, 3>::smem(a.TLB) <= kMaxSmem;
+  const bool fit2 = TcCfg<K, S, 2>::smem(a.TLB) <= kMaxSmem;
+  if (!fit2) return DISCO_ERR_UNSUPPORTED;
   auto enc = encode_fn();
   if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const int Hin = psi->grid_in.nlat, Win = psi->grid_in.nlon;
   CUtensorMap map;
   cuuint64_t dims[3] = {(cuuint64_t)Win, (cuuint64_t)Hin, (cuuint64_t)BC};
   cuuint64_t strides[2] = {(cuuint64_t)Win * 2, (cuuint64_t)Hin * Win * 2};
@@ -346,24 +439,7 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
-  TcArgs a;
-  a.X = (__nv_bfloat16*)X;
-  a.val = psi->val;
-  a.runs = psi->runs;
-  a.run_ptr = psi->run_ptr;
-  a.row_order = psi->row_order;
-  a.BC = BC;
-  a.Hout = psi->grid_out.nlat;
-  a.Wout = psi->grid_out.nlon;
-  a.Win = Win;
-  a.Kp = psi->K_pad;
-  auto kern = fwd_tc_kernel<K, S>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) !=
-      cudaSuccess)
-    return check_launch("disco_fwd (tensor cores) attribute");
-  dim3 grid((a.Wout + kTW * Cfg::NT - 1) / (kTW * Cfg::NT), (BC + 127) / 128, a.Hout);
-  kern<<<grid, kThreads, Cfg::kSmem, st>>>(map, a);
-  return check_launch("disco_fwd (tensor cores)");
+  return fit3 ? launch_tc_stages<K, S, 3>(psi, map, a, st) : launch_tc_stages<K, S, 2>(psi, map, a, st);
 }
 
 }  // namespace

@@ -31,6 +31,11 @@ int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaSt
 // ORs the tensor-core unit's status word into *v (device already synchronised).
 cudaError_t tc_status(int32_t* v, bool clear);
 
+// Transpose contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
+// without launching, for shapes that path does not take.
+int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st);
+cudaError_t btc_status(int32_t* v, bool clear);
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

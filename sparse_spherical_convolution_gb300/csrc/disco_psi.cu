@@ -113,15 +113,36 @@ __device__ __host__ inline int run_len(int m, int W) {
   return 2 * m + 1;
 }
 
+constexpr int kRS = 5;  // per-row totals before the ring counts
+
+// run extent: offsets dlo..dhi (full ring of even width: -W/2 .. W/2 - 1)
+__device__ __host__ inline void run_extent(int m, int W, int* dlo, int* dhi) {
+  const int len = run_len(m, W);
+  *dlo = (len == W) ? -(W / 2) : -m;
+  *dhi = *dlo + len - 1;
+}
+__device__ __host__ inline int floordiv(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+__device__ __host__ inline int ceildiv(int a, int b) { return -floordiv(-a, b); }
+// table row lengths of a run (elements, multiples of 8)
+__device__ __host__ inline int ftab_len(int m, int W) { return (run_len(m, W) + 16 + 7) & ~7; }
+__device__ __host__ inline int btab_len(int m, int W, int s) {
+  int dlo, dhi;
+  run_extent(m, W, &dlo, &dhi);
+  const int EH = floordiv(dhi, s), EL = ceildiv(dlo - s + 1, s);
+  return (EH - EL + 1 + 16 + 7) & ~7;
+}
+
 struct Workspace {
   int32_t* mtab;      // [Hout][Hin]
   int32_t* ringcnt;   // [Hout][Hin][R]
   double* hq;         // [Hout][Hin][R]
-  int32_t* rowsum;    // [Hout][3 + R]: len, runs, hval rows, ring counts
+  int32_t* rowsum;    // [Hout][5 + R]: len, runs, hval rows, ftab, btab elements, ring counts
   int32_t* off;       // [Hout][Hin]: entry offset of the run inside its row
   int32_t* runidx;    // [Hout][Hin]
   int32_t* csroff;    // [Hout][Hin][R]
   int32_t* hofftab;   // [Hout][Hin]
+  int32_t* ftofftab;  // [Hout][Hin]: forward table offset of the run
+  int32_t* btofftab;  // [Hout][Hin]: transpose table offset of the run
   double* norm;       // [Hout][R]
   int32_t* tcount;    // [Hin + 1]
 };
@@ -139,7 +160,9 @@ size_t carve_workspace(const PsiGeom& g, char* base, Workspace* ws) {
   w.mtab = (int32_t*)take(HH * 4);
   w.ringcnt = (int32_t*)take(HH * g.R * 4);
   w.hq = (double*)take(HH * g.R * 8);
-  w.rowsum = (int32_t*)take((size_t)g.Hout * (3 + g.R) * 4);
+  w.rowsum = (int32_t*)take((size_t)g.Hout * (kRS + g.R) * 4);
+  w.ftofftab = (int32_t*)take(HH * 4);
+  w.btofftab = (int32_t*)take(HH * 4);
   w.off = (int32_t*)take(HH * 4);
   w.runidx = (int32_t*)take(HH * 4);
   w.csroff = (int32_t*)take(HH * g.R * 4);
@@ -192,7 +215,8 @@ __global__ void count_kernel(PsiGeom g, Workspace ws) {
 __global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
   int ho = blockIdx.x * blockDim.x + threadIdx.x;
   if (ho >= g.Hout) return;
-  int len = 0, runs = 0, hrows = 0, rc[kMaxRad] = {0};
+  int len = 0, runs = 0, hrows = 0, ft = 0, bt = 0, rc[kMaxRad] = {0};
+  const int s = g.Win / g.Wout;
   for (int hi = 0; hi < g.Hin; ++hi) {
     size_t t = (size_t)ho * g.Hin + hi;
     int m = ws.mtab[t];
@@ -200,19 +224,25 @@ __global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
     len += run_len(m, g.Win);
     runs += 1;
     hrows += m + 1;  // pair steps delta = 0 .. m (m = W/2 includes the antipodal step)
+    ft += g.K * ftab_len(m, g.Win);
+    bt += g.K * s * btab_len(m, g.Win, s);
     for (int r = 0; r < g.R; ++r) rc[r] += ws.ringcnt[t * g.R + r];
   }
-  int32_t* o = ws.rowsum + (size_t)ho * (3 + g.R);
+  int32_t* o = ws.rowsum + (size_t)ho * (kRS + g.R);
   o[0] = len;
   o[1] = runs;
   o[2] = hrows;
-  for (int r = 0; r < g.R; ++r) o[3 + r] = rc[r];
+  o[3] = ft;
+  o[4] = bt;
+  for (int r = 0; r < g.R; ++r) o[kRS + r] = rc[r];
 }
 
 struct PsiOut {
   int32_t *row_ptr, *idx, *csr_row_ptr, *csr_col, *run_ptr, *trun_ptr, *truns, *row_order;
   float *val, *csr_val, *hval;
   disco_run* runs;
+  int32_t *ftab_off, *btab_off;
+  uint16_t *ftab, *btab;
 };
 
 __device__ __forceinline__ int ring_of(int kind, int k) { return kind == 1 ? k / 3 : k; }
@@ -224,7 +254,7 @@ __global__ void scan_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   p.row_ptr[0] = 0;
   p.run_ptr[0] = 0;
   for (int ho = 0; ho < g.Hout; ++ho) {
-    const int32_t* o = ws.rowsum + (size_t)ho * (3 + g.R);
+    const int32_t* o = ws.rowsum + (size_t)ho * (kRS + g.R);
     e += o[0];
     r += o[1];
     p.row_ptr[ho + 1] = e;
@@ -234,7 +264,7 @@ __global__ void scan_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   p.csr_row_ptr[0] = 0;
   for (int k = 0; k < g.K; ++k)
     for (int ho = 0; ho < g.Hout; ++ho) {
-      c += ws.rowsum[(size_t)ho * (3 + g.R) + 3 + ring_of(g.kind, k)];
+      c += ws.rowsum[(size_t)ho * (kRS + g.R) + kRS + ring_of(g.kind, k)];
       p.csr_row_ptr[k * g.Hout + ho + 1] = c;
     }
 }
@@ -247,8 +277,13 @@ __global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   int32_t off = 0, run = p.run_ptr[ho];
   // pair-weight rows: runs are numbered globally in (ho, hi) order, so the
   // hval offset of a run is the running total over all earlier runs.
-  int32_t hoff = 0;
-  for (int h2 = 0; h2 < ho; ++h2) hoff += ws.rowsum[(size_t)h2 * (3 + g.R) + 2];
+  int32_t hoff = 0, foff = 0, boff = 0;
+  for (int h2 = 0; h2 < ho; ++h2) {
+    hoff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 2];
+    foff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 3];
+    boff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 4];
+  }
+  const int s = g.Win / g.Wout;
   int32_t rc[kMaxRad] = {0};
   double nrm[kMaxRad] = {0};
   for (int hi = 0; hi < g.Hin; ++hi) {
@@ -257,11 +292,15 @@ __global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     ws.off[t] = off;
     ws.runidx[t] = m >= 0 ? run : -1;
     ws.hofftab[t] = hoff;
+    ws.ftofftab[t] = foff;
+    ws.btofftab[t] = boff;
     for (int r = 0; r < g.R; ++r) ws.csroff[t * g.R + r] = rc[r];
     if (m < 0) continue;
     off += run_len(m, g.Win);
     run += 1;
     hoff += m + 1;
+    foff += g.K * ftab_len(m, g.Win);
+    boff += g.K * s * btab_len(m, g.Win, s);
     for (int r = 0; r < g.R; ++r) {
       rc[r] += ws.ringcnt[t * g.R + r];
       nrm[r] = __dadd_rn(nrm[r], ws.hq[t * g.R + r]);
@@ -352,6 +391,53 @@ __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   }
 }
 
+// bf16 tables of each run (forward and polyphase transpose), from val
+__global__ void table_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  const int ho = blockIdx.x;
+  const int s = g.Win / g.Wout;
+  for (int hi = blockIdx.y; hi < g.Hin; hi += gridDim.y) {
+    const size_t t = (size_t)ho * g.Hin + hi;
+    const int m = ws.mtab[t];
+    if (m < 0) continue;
+    const int r = ws.runidx[t];
+    const int e0 = p.row_ptr[ho] + ws.off[t];
+    int dlo, dhi;
+    run_extent(m, g.Win, &dlo, &dhi);
+    const int tlf = ftab_len(m, g.Win), tlb = btab_len(m, g.Win, s);
+    const int foff = ws.ftofftab[t], boff = ws.btofftab[t];
+    if (threadIdx.x == 0) {
+      p.ftab_off[r] = foff;
+      p.btab_off[r] = boff;
+    }
+    for (int i = threadIdx.x; i < g.K * tlf; i += blockDim.x) {
+      const int k = i / tlf, x = i - k * tlf;
+      const int d = dlo + x - 8;
+      const float v = (d >= dlo && d <= dhi) ? p.val[(size_t)(e0 + d - dlo) * g.Kp + k] : 0.f;
+      p.ftab[foff + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+    const int EH = floordiv(dhi, s);
+    for (int i = threadIdx.x; i < g.K * s * tlb; i += blockDim.x) {
+      const int row = i / tlb, x = i - row * tlb;
+      const int k = row / s, ph = row - k * s;
+      const int e = EH - (x - 8);
+      const int d = s * e + ph;
+      const float v = (x >= 8 && d >= dlo && d <= dhi) ? p.val[(size_t)(e0 + d - dlo) * g.Kp + k] : 0.f;
+      p.btab[boff + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
+}
+
+__global__ void table_tail_kernel(PsiGeom g, Workspace ws, PsiOut p, int32_t nruns) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int32_t f = 0, b = 0;
+  for (int ho = 0; ho < g.Hout; ++ho) {
+    f += ws.rowsum[(size_t)ho * (kRS + g.R) + 3];
+    b += ws.rowsum[(size_t)ho * (kRS + g.R) + 4];
+  }
+  p.ftab_off[nruns] = f;
+  p.btab_off[nruns] = b;
+}
+
 // transposed run list: count per input row, scan, fill (ho ascending)
 __global__ void tcount_kernel(PsiGeom g, Workspace ws) {
   int hi = blockIdx.x * blockDim.x + threadIdx.x;
@@ -385,10 +471,10 @@ __global__ void tfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
 __global__ void order_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   int ho = blockIdx.x * blockDim.x + threadIdx.x;
   if (ho >= g.Hout) return;
-  int my = ws.rowsum[(size_t)ho * (3 + g.R)];
+  int my = ws.rowsum[(size_t)ho * (kRS + g.R)];
   int rank = 0;
   for (int h2 = 0; h2 < g.Hout; ++h2) {
-    int o = ws.rowsum[(size_t)h2 * (3 + g.R)];
+    int o = ws.rowsum[(size_t)h2 * (kRS + g.R)];
     rank += (o > my) || (o == my && h2 < ho);
   }
   p.row_order[rank] = ho;
@@ -447,6 +533,10 @@ size_t carve_psi(const disco_psi* psi, char* base, PsiOut* out) {
   p.truns = (int32_t*)take((size_t)psi->nruns * 4);
   p.hval = (float*)take((size_t)psi->nhval * psi->K_pad * 4);
   p.row_order = (int32_t*)take((size_t)Hout * 4);
+  p.ftab_off = (int32_t*)take((size_t)(psi->nruns + 1) * 4);
+  p.ftab = (uint16_t*)take((size_t)psi->nftab * 2);
+  p.btab_off = (int32_t*)take((size_t)(psi->nruns + 1) * 4);
+  p.btab = (uint16_t*)take((size_t)psi->nbtab * 2);
   if (out) *out = p;
   return o;
 }
@@ -486,21 +576,24 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
   if ((st = check_launch("psi count"))) return st;
   rowsum_kernel<<<(g.Hout + 127) / 128, 128, 0, s>>>(g, ws);
   if ((st = check_launch("psi rowsum"))) return st;
-  std::vector<int32_t> rs((size_t)g.Hout * (3 + g.R));
+  std::vector<int32_t> rs((size_t)g.Hout * (kRS + g.R));
   cudaError_t ce = cudaMemcpyAsync(rs.data(), ws.rowsum, rs.size() * 4, cudaMemcpyDeviceToHost, s);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
   if (ce != cudaSuccess) return fail(DISCO_ERR_CUDA, "psi plan copy: %s", cudaGetErrorString(ce));
-  int64_t nnz = 0, nruns = 0, nhval = 0, nnz_csr = 0;
+  int64_t nnz = 0, nruns = 0, nhval = 0, nnz_csr = 0, nftab = 0, nbtab = 0;
   int32_t max_row = 0;
   for (int ho = 0; ho < g.Hout; ++ho) {
-    const int32_t* o = &rs[(size_t)ho * (3 + g.R)];
+    const int32_t* o = &rs[(size_t)ho * (kRS + g.R)];
     nnz += o[0];
     nruns += o[1];
     nhval += o[2];
+    nftab += o[3];
+    nbtab += o[4];
     if (o[0] > max_row) max_row = o[0];
-    for (int k = 0; k < g.K; ++k) nnz_csr += o[3 + (g.kind == 1 ? k / 3 : k)];
+    for (int k = 0; k < g.K; ++k) nnz_csr += o[kRS + (g.kind == 1 ? k / 3 : k)];
   }
-  if (nnz >= ((int64_t)1 << 31) / 16 || nnz_csr >= ((int64_t)1 << 31))
+  if (nnz >= ((int64_t)1 << 31) / 16 || nnz_csr >= ((int64_t)1 << 31) || nftab >= ((int64_t)1 << 31) ||
+      nbtab >= ((int64_t)1 << 31))
     return fail(DISCO_ERR_UNSUPPORTED, "psi too large for int32 offsets");
   memset(psi, 0, sizeof(*psi));
   psi->grid_in = *grid_in;
@@ -514,6 +607,8 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
   psi->nnz_csr = nnz_csr;
   psi->nruns = nruns;
   psi->nhval = nhval;
+  psi->nftab = nftab;
+  psi->nbtab = nbtab;
   psi->bytes = carve_psi(psi, nullptr, nullptr);
   return DISCO_OK;
 }
@@ -546,6 +641,10 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   if ((st = check_launch("psi offsets"))) return st;
   fill_kernel<<<g.Hout, 64, 0, s>>>(g, ws, p);
   if ((st = check_launch("psi fill"))) return st;
+  table_kernel<<<dim3(g.Hout, 32), 128, 0, s>>>(g, ws, p);
+  if ((st = check_launch("psi tables"))) return st;
+  table_tail_kernel<<<1, 1, 0, s>>>(g, ws, p, (int32_t)psi->nruns);
+  if ((st = check_launch("psi table tail"))) return st;
   tcount_kernel<<<(g.Hin + tb - 1) / tb, tb, 0, s>>>(g, ws);
   if ((st = check_launch("psi tcount"))) return st;
   tscan_kernel<<<1, 1, 0, s>>>(g, ws, p);
@@ -566,5 +665,9 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   psi->truns = p.truns;
   psi->hval = p.hval;
   psi->row_order = p.row_order;
+  psi->ftab_off = p.ftab_off;
+  psi->ftab = p.ftab;
+  psi->btab_off = p.btab_off;
+  psi->btab = p.btab;
   return DISCO_OK;
 }

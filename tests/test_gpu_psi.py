@@ -104,3 +104,34 @@ def test_runs_are_consistent_with_union_layout(lib, case):
     assert sorted(order.tolist()) == list(range(go[0]))
     work = np.diff(row_ptr)[order]
     assert np.all(np.diff(work) <= 0)
+    _check_tables(psi, runs, val, gi, go)
+
+
+def _bf16_bits(v):
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+def _check_tables(psi, runs, val, gi, go):
+    """Forward and polyphase transpose tables hold exactly the bf16-rounded
+    union values at the documented positions and zeros elsewhere."""
+    K, W, s = psi.c.K, gi[1], gi[1] // go[1]
+    ftab, foff = psi.tensor("ftab").cpu().numpy(), psi.tensor("ftab_off").cpu().numpy()
+    btab, boff = psi.tensor("btab").cpu().numpy(), psi.tensor("btab_off").cpu().numpy()
+    assert foff[-1] == psi.c.nftab and boff[-1] == psi.c.nbtab
+    for r, (ho, hi, D, hoff, e0, ln, npair, anti) in enumerate(runs):
+        dlo = -(W // 2) if ln == W else -npair
+        dhi = dlo + ln - 1
+        vb = _bf16_bits(val[e0:e0 + ln, :K])            # [len, K], offsets dlo..dhi
+        TL = (ln + 16 + 7) // 8 * 8
+        want = np.zeros((K, TL), np.int16)
+        want[:, 8:8 + ln] = vb.T
+        assert np.array_equal(ftab[foff[r]:foff[r] + K * TL].reshape(K, TL), want)
+        EH, EL = dhi // s, -((-(dlo - s + 1)) // s)
+        TB = (EH - EL + 1 + 16 + 7) // 8 * 8
+        wantb = np.zeros((K, s, TB), np.int16)
+        for p in range(s):
+            for e in range(EL, EH + 1):
+                d = s * e + p
+                if dlo <= d <= dhi:
+                    wantb[:, p, 8 + EH - e] = vb[d - dlo]
+        assert np.array_equal(btab[boff[r]:boff[r] + K * s * TB].reshape(K, s, TB), wantb)
