@@ -152,18 +152,19 @@ def run_ours(args):
     gx = torch.empty(sh["x"], dtype=dt, device=dev)
     y = torch.empty(sh["y"], dtype=dt, device=dev)
     gx2 = torch.empty(sh["x"], dtype=dt, device=dev)
-    wsb = d.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, C)
-    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    wsb = max(d.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, C),
+              d.disco_fused_conv_workspace_bytes(psi.c, B, C))
+    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)  # shared: the calls run in sequence
     stream = torch.cuda.current_stream(dev)
     alg = algorithmic(w, psi.c)
 
     calls = [
         ("fwd", lambda: d.disco_fwd(psi.c, x, X, B, C, stream)),
         ("bwd", lambda: d.disco_bwd(psi.c, G, gx, B, C, stream)),
-        ("fused", lambda: d.disco_fused_conv(psi.c, x, Wt, y, B, C, Co, stream)),
+        ("fused", lambda: d.disco_fused_conv(psi.c, x, Wt, y, B, C, Co, wsp, stream)),
         ("fused_bwd", lambda: d.disco_fused_conv_bwd_input(psi.c, dy, Wt, gx2, B, C, Co, wsp, stream)),
     ]
-    launches_per_step = 5  # fwd, bwd, fused, dX gemm + transpose
+    launches_per_step = 6  # fwd, bwd, fused (contraction + einsum), fused bwd (dX gemm + transpose)
 
     def step(ev=None):
         for i, (_, fn) in enumerate(calls):

@@ -193,16 +193,27 @@ DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B,
 DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
+/* Device workspace bytes of disco_fused_conv: the bf16 intermediate
+   X[B, Cin, K, H_out, W_out] when the tensor-core contraction takes the shape
+   (bf16, W_in % 8 == 0, s in {1, 2}, K <= 9), else 0 (no workspace needed). */
+DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
+                                                  disco_dtype dtype);
+
 /* Fused convolution (§Architecture snapshot "_disco_s2_fused_conv_optimized:
    contraction + einsum"):  y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo]
-   with X the forward contraction, which never leaves the chip: it is built
-   in shared memory as bf16 and contracted on the tcgen05 tensor cores with
-   fp32 accumulation in tensor memory.
+   with X the forward contraction, in one call:
+     - where the tensor-core contraction takes the shape, X is produced by it
+       into `workspace` (bf16, disco_fused_conv_workspace_bytes bytes) and the
+       einsum runs as a tcgen05 GEMM (M = 128 pixels, N = Cout, K = Cin*K);
+     - otherwise X is built in shared memory by the CUDA-core gather, 16 input
+       channels at a time, and contracted on the tcgen05 tensor cores without
+       leaving the chip (workspace unused; needs Cin % 16 == 0).
+   Accumulation is fp32 (TMEM); X is rounded to bf16 before the einsum.
    x: [B, Cin, H_in, W_in] bf16, W: [Cout, Cin, K] bf16, y: [B, Cout, H_out, W_out] bf16.
-   dtype must be DISCO_BF16; Cin % 16 == 0; Cout <= 256. */
+   dtype must be DISCO_BF16; Cout <= 256. */
 DISCO_API int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
                      int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
-                     void* stream);
+                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Device workspace bytes of disco_fused_conv_bwd_input (the bf16 intermediate
    dX[B, Cin, K, H_out, W_out]). */

@@ -18,8 +18,8 @@ from . import build as _build_mod
 __all__ = [
     "DiscoError", "disco_grid", "disco_basis", "disco_run", "disco_psi", "Psi",
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
-    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
-    "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
+    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv_workspace_bytes",
+    "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_device_status", "library_path",
     "load_library", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
@@ -30,8 +30,8 @@ DISCO_F32, DISCO_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
-    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv",
-    "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
+    "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv_workspace_bytes",
+    "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_device_status",
 ]
 
@@ -100,8 +100,10 @@ def load_library():
     lib.disco_fwd.argtypes = [PP, P, P, I32, I32, ctypes.c_int, P]
     lib.disco_bwd.restype = ctypes.c_int
     lib.disco_bwd.argtypes = [PP, P, P, I32, I32, ctypes.c_int, P]
+    lib.disco_fused_conv_workspace_bytes.restype = SZ
+    lib.disco_fused_conv_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
     lib.disco_fused_conv.restype = ctypes.c_int
-    lib.disco_fused_conv.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P]
+    lib.disco_fused_conv.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_fused_conv_bwd_input_workspace_bytes.restype = SZ
     lib.disco_fused_conv_bwd_input_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
     lib.disco_fused_conv_bwd_input.restype = ctypes.c_int
@@ -198,9 +200,15 @@ def disco_bwd(psi: disco_psi, G, gx, B: int, C: int, stream=None) -> None:
                                     _stream(stream)))
 
 
-def disco_fused_conv(psi: disco_psi, x, W, y, B: int, Cin: int, Cout: int, stream=None) -> None:
+def disco_fused_conv_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:
+    return load_library().disco_fused_conv_workspace_bytes(ctypes.byref(psi), B, Cin, dtype)
+
+
+def disco_fused_conv(psi: disco_psi, x, W, y, B: int, Cin: int, Cout: int, workspace=None,
+                     stream=None) -> None:
+    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load_library().disco_fused_conv(ctypes.byref(psi), _ptr(x), _ptr(W), _ptr(y), B, Cin,
-                                           Cout, _dtype(x), _stream(stream)))
+                                           Cout, _dtype(x), _ptr(workspace), nws, _stream(stream)))
 
 
 def disco_fused_conv_bwd_input_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:

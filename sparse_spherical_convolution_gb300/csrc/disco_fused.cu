@@ -441,6 +441,155 @@ __global__ void __launch_bounds__(kGThreads, 2) dx_gemm_kernel(const GemmArgs a)
   }
 }
 
+// ------------------------------------------------------ y = W X (einsum) --
+//
+// D[p, o] = sum_ck X[b, ck, p] * W[o, ck]   (p = pixel ho*W_out + wo, ck = c*K + k)
+// M = 128 pixels, N = Cout (<= 256, one tile), K = Cin*K in chunks of 64,
+// two-stage pipeline.  A = X^T tile: each thread gathers 8 consecutive ck of
+// one pixel (lanes on consecutive pixels) into one 16-byte core-matrix row;
+// B = W tile: 16-byte rows of W[o][ck] as they are (already K-major).
+// Epilogue: lane = pixel, so each column store of y is coalesced.
+
+constexpr int kEN = 256;                        // max Cout per tile
+constexpr int kETileB = kEN * kGK * 2;          // 32 KB
+constexpr int kEStage = kGTileA + kETileB;
+constexpr size_t kESmem = 2 * (size_t)kEStage + 64;
+
+struct EinArgs {
+  const __nv_bfloat16* X;   // [B][CK][P]
+  const __nv_bfloat16* W;   // [Cout][CK]
+  __nv_bfloat16* y;         // [B][Cout][P]
+  int Cout, CK, Npad;       // Npad: Cout rounded up to 16
+  int64_t P;
+};
+
+__global__ void __launch_bounds__(kGThreads, 2) einsum_gemm_kernel(const EinArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kEStage);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t p0 = (int64_t)blockIdx.x * kGM;
+  const int b = blockIdx.y;
+  const int nk = (a.CK + kGK - 1) / kGK;
+  const __nv_bfloat16* Xb = a.X + (size_t)b * a.CK * a.P;
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, kEN);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  bool ok = true;
+  const bool vec_w = (a.CK % 8) == 0;
+
+  for (int kc = 0; kc < nk; ++kc) {
+    const int s = kc & 1;
+    uint8_t* sA = smem + s * kEStage;
+    uint8_t* sB = sA + kGTileA;
+    if (kc >= 2) {
+      if (!mbar_wait(&bars[s], ((kc - 2) >> 1) & 1, kWaitLimit)) {
+        if (tid == 0) flag_status(kStatusGemmTimeout);
+        ok = false;
+      }
+    }
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    const int c_base = kc * kGK;
+    // A: (row p, k ck) <- X[ck][p]
+    for (int i = tid; i < kGM * (kGK / 8); i += kGThreads) {
+      const int pl = i % kGM, cg = i / kGM;
+      const int64_t p = p0 + pl;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int ck = c_base + cg * 8 + e;
+        __nv_bfloat16 v0 = __float2bfloat16_rn(0.f), v1 = v0;
+        if (p < a.P) {
+          if (ck < a.CK) v0 = Xb[(size_t)ck * a.P + p];
+          if (ck + 1 < a.CK) v1 = Xb[(size_t)(ck + 1) * a.P + p];
+        }
+        __nv_bfloat162 p2;
+        p2.x = v0;
+        p2.y = v1;
+        w[e >> 1] = *reinterpret_cast<uint32_t*>(&p2);
+      }
+      *reinterpret_cast<uint4*>(sA + kmajor_off(pl, cg * 8, kGSBO)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    // B: (row o, k ck) <- W[o][ck], 16-byte pieces
+    for (int i = tid; i < a.Npad * (kGK / 8); i += kGThreads) {
+      const int o = i / (kGK / 8), cg = i % (kGK / 8);
+      const int ck = c_base + cg * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (o < a.Cout) {
+        if (vec_w && ck + 8 <= a.CK) {
+          v = *reinterpret_cast<const uint4*>(a.W + (size_t)o * a.CK + ck);
+        } else {
+          __align__(16) __nv_bfloat16 t[8];
+          for (int e = 0; e < 8; ++e)
+            t[e] = (ck + e < a.CK) ? a.W[(size_t)o * a.CK + ck + e] : __float2bfloat16_rn(0.f);
+          v = *reinterpret_cast<uint4*>(t);
+        }
+      }
+      *reinterpret_cast<uint4*>(sB + kmajor_off(o, cg * 8, kGSBO)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(kGM, a.Npad);
+#pragma unroll
+      for (int ks = 0; ks < kGK / 16; ++ks) {
+        const uint64_t ad = smem_desc(smem_u32(sA) + ks * 256, 128, kGSBO);
+        const uint64_t bd = smem_desc(smem_u32(sB) + ks * 256, 128, kGSBO);
+        umma_bf16(tmem, ad, bd, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
+      }
+      umma_commit(&bars[s]);
+    }
+  }
+  {
+    const int last = nk - 1;
+    bool done = mbar_wait(&bars[last & 1], (last >> 1) & 1, kWaitLimit);
+    done = __syncthreads_and(done) != 0;
+    if (!done && tid == 0) flag_status(kStatusGemmTimeout);
+    ok = ok && done;
+  }
+  tc_fence_after();
+  if (ok) {
+    // 8 warps: lane quarter = warp % 4, column half = warp / 4
+    const int q = warp & 3, half = warp >> 2;
+    const int64_t p = p0 + q * 32 + lane;
+    const int ncols = a.Npad / 2;
+#pragma unroll 1
+    for (int j = 0; j < ncols / 16; ++j) {
+      float v[16];
+      const int c0 = half * ncols + j * 16;
+      tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+      if (p < a.P) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int o = c0 + i;
+          if (o < a.Cout) a.y[((size_t)b * a.Cout + o) * a.P + p] = __float2bfloat16_rn(v[i]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kEN);
+  }
+}
+
 int check_fused_common(const disco_psi* psi, const void* a, const void* W, const void* out,
                        int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype) {
   int st = check_psi(psi);
@@ -462,13 +611,52 @@ int check_fused_common(const disco_psi* psi, const void* a, const void* W, const
 
 using namespace disco;
 
+// Tensor-core path of disco_fused_conv: X = contraction into the workspace
+// (bf16), then the einsum on the tensor cores.
+static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y, int32_t B, int32_t Cin,
+                    int32_t Cout, void* X, cudaStream_t s) {
+  int st = fwd_tensor_core(psi, x, X, B * Cin, s);
+  if (st) return st;
+  EinArgs e;
+  e.X = (const __nv_bfloat16*)X;
+  e.W = (const __nv_bfloat16*)W;
+  e.y = (__nv_bfloat16*)y;
+  e.Cout = Cout;
+  e.CK = Cin * psi->K;
+  e.Npad = (Cout + 31) / 32 * 32;  // the epilogue splits N into two halves of 16-column steps
+  e.P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
+  if (cudaFuncSetAttribute(einsum_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kESmem) !=
+      cudaSuccess)
+    return check_launch("einsum attribute");
+  dim3 grid((unsigned)((e.P + kGM - 1) / kGM), B);
+  if (grid.x > 0x7fffffffu || B > 65535) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
+  einsum_gemm_kernel<<<grid, kGThreads, kESmem, s>>>(e);
+  return check_launch("einsum");
+}
+
+extern "C" size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
+                                                   disco_dtype dtype) {
+  if (!psi || B < 1 || Cin < 1 || dtype != DISCO_BF16 || !fwd_tc_supported(psi, B * Cin)) return 0;
+  return (size_t)B * Cin * psi->K * psi->grid_out.nlat * psi->grid_out.nlon * 2;
+}
+
 extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
                                 int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
-                                void* stream) {
+                                void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_fused_common(psi, x, W, y, B, Cin, Cout, dtype);
   if (st) return st;
-  if (Cin % kFCC != 0) return fail(DISCO_ERR_UNSUPPORTED, "Cin must be a multiple of %d", kFCC);
   if (Cout > 256) return fail(DISCO_ERR_UNSUPPORTED, "Cout must be <= 256");
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t need = disco_fused_conv_workspace_bytes(psi, B, Cin, dtype);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    if (!aligned16(workspace)) return fail(DISCO_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    return fused_tc(psi, x, W, y, B, Cin, Cout, workspace, s);
+  }
+  // shapes the tensor-core contraction does not take: X built on chip by the
+  // CUDA-core gather, einsum on the tensor cores
+  if (Cin % kFCC != 0) return fail(DISCO_ERR_UNSUPPORTED, "Cin must be a multiple of %d", kFCC);
   FusedArgs a;
   a.x = (const __nv_bfloat16*)x;
   a.W = (const __nv_bfloat16*)W;
@@ -486,7 +674,6 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
   a.runs = psi->runs;
   a.hval = psi->hval;
   a.row_order = psi->row_order;
-  cudaStream_t s = (cudaStream_t)stream;
   return psi->s == 1 ? dispatch_fused<1>(psi->basis.kind, psi->K, a, s)
                      : dispatch_fused<2>(psi->basis.kind, psi->K, a, s);
 }

@@ -442,6 +442,12 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
   return fit3 ? launch_tc_stages<K, S, 3>(psi, map, a, st) : launch_tc_stages<K, S, 2>(psi, map, a, st);
 }
 
+template <int K, int S>
+bool fits_tc(const disco_psi* psi) {
+  const int TLB = (psi->grid_in.nlon + 16 + 7) & ~7;
+  return TcCfg<K, S, 2>::smem(TLB) <= 227 * 1024;
+}
+
 }  // namespace
 
 // Reads (and optionally clears) this unit's status word; the caller has
@@ -457,12 +463,30 @@ cudaError_t tc_status(int32_t* v, bool clear) {
   return e;
 }
 
+// True when fwd_tensor_core takes this psi and channel count.
+bool fwd_tc_supported(const disco_psi* psi, int BC) {
+  if (psi->grid_in.nlon % 8 != 0 || (psi->s != 1 && psi->s != 2) || BC < 1 || BC > 65535 * 128 ||
+      !psi->ftab || !psi->ftab_off || psi->K < 1 || psi->K > 9)
+    return false;
+#define DISCO_TFIT(KK) \
+  if (psi->K == KK) return psi->s == 1 ? fits_tc<KK, 1>(psi) : fits_tc<KK, 2>(psi);
+  DISCO_TFIT(1)
+  DISCO_TFIT(2)
+  DISCO_TFIT(3)
+  DISCO_TFIT(4)
+  DISCO_TFIT(5)
+  DISCO_TFIT(6)
+  DISCO_TFIT(7)
+  DISCO_TFIT(8)
+  DISCO_TFIT(9)
+#undef DISCO_TFIT
+  return false;
+}
+
 // Forward contraction on the tensor cores; returns DISCO_ERR_UNSUPPORTED
 // (without launching) for shapes this path does not take.
 int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
-  const int Win = psi->grid_in.nlon;
-  if (Win % 8 != 0 || (psi->s != 1 && psi->s != 2) || BC > 65535 * 128)
-    return DISCO_ERR_UNSUPPORTED;
+  if (!fwd_tc_supported(psi, BC)) return DISCO_ERR_UNSUPPORTED;
   const int K = psi->K;
 #define DISCO_TCASE(KK)                                                               \
   if (K == KK) return psi->s == 1 ? launch_tc<KK, 1>(psi, x, X, BC, st)              \

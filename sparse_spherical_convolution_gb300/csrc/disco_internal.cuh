@@ -27,6 +27,7 @@ int check_psi(const disco_psi* psi);
 // Forward contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
 // without launching, for shapes that path does not take.
 int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st);
+bool fwd_tc_supported(const disco_psi* psi, int BC);
 
 // ORs the tensor-core unit's status word into *v (device already synchronised).
 cudaError_t tc_status(int32_t* v, bool clear);

@@ -63,6 +63,6 @@ def test_hot_calls_reject_unbuilt_psi_before_any_launch(lib):
     assert so.disco_fwd(ctypes.byref(empty), None, None, 1, 1, 1, None) == -1
     assert "psi" in lib.disco_last_error()
     assert so.disco_bwd(None, None, None, 1, 1, 1, None) == -1
-    assert so.disco_fused_conv(ctypes.byref(empty), None, None, None, 1, 16, 16, 1, None) == -1
+    assert so.disco_fused_conv(ctypes.byref(empty), None, None, None, 1, 16, 16, 1, None, 0, None) == -1
     assert so.disco_fused_conv_bwd_input(ctypes.byref(empty), None, None, None, 1, 16, 16, 1,
                                          None, 0, None) == -1

@@ -33,6 +33,8 @@ SMALL = [
     ((17, 32, 1), (9, 16, 1), 1, 2, 3 * math.pi / 8, 1, 48, 256),         # poles, s = 2, K = 6
     ((37, 200, 1), (37, 200, 1), 1, 3, 4 * math.pi / 36, 1, 16, 64),      # ragged 64-column tiles
     ((10, 24, 0), (10, 12, 0), 0, 1, 0.9, 3, 16, 20),                      # K = 1, narrow ring
+    ((16, 36, 0), (16, 36, 0), 1, 3, 2 * math.pi / 16, 1, 16, 40),        # W_in % 8 != 0: on-chip path
+    ((32, 64, 0), (16, 32, 0), 1, 3, 3 * math.pi / 16, 1, 24, 8),         # Cin % 16 != 0 (workspace path)
 ]
 
 
@@ -46,7 +48,9 @@ def _inputs(B, Cin, Cout, K, gi, go, seed):
 
 def _run_fused(lib, psi, x, W, B, Cin, Cout, go):
     y = torch.full((B, Cout, go[0], go[1]), float("nan"), dtype=BF, device="cuda")
-    lib.disco_fused_conv(psi.c, x, W, y, B, Cin, Cout)
+    nws = lib.disco_fused_conv_workspace_bytes(psi.c, B, Cin)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda") if nws else None
+    lib.disco_fused_conv(psi.c, x, W, y, B, Cin, Cout, ws)
     return y
 
 
@@ -149,10 +153,17 @@ def test_fused_rejects_unsupported(lib):
     W = torch.zeros((8, 8, 3), dtype=BF, device="cuda")
     y = torch.zeros((1, 8, 16, 32), dtype=BF, device="cuda")
     with pytest.raises(lib.DiscoError) as e:
-        lib.disco_fused_conv(psi.c, x, W, y, 1, 8, 8)  # Cin % 16 != 0
-    assert e.value.status == -2
+        lib.disco_fused_conv(psi.c, x, W, y, 1, 8, 8)  # no workspace for the tensor-core path
+    assert e.value.status == -7
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_fused_conv(psi.c, x.float(), W, y, 1, 8, 8)  # fp32
+    assert e.value.status == -2
+    psi36 = lib.Psi((16, 36, 0), (16, 36, 0), 0, 3, 2 * math.pi / 16)  # on-chip path
+    x36 = torch.zeros((1, 8, 16, 36), dtype=BF, device="cuda")
+    y36 = torch.zeros((1, 8, 16, 36), dtype=BF, device="cuda")
+    assert lib.disco_fused_conv_workspace_bytes(psi36.c, 1, 8) == 0
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_fused_conv(psi36.c, x36, W, y36, 1, 8, 8)  # Cin % 16 != 0 on the on-chip path
     assert e.value.status == -2
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(lib.DiscoError) as e:
