@@ -91,6 +91,17 @@ typedef struct {
   int32_t anti;  /* 1 if the run holds the unpaired antipodal column */
 } disco_run;
 
+/* One (input-row group, output row) entry of the transpose tables; see
+   disco_psi.grp_ptr. */
+typedef struct {
+  int32_t ho;   /* output row */
+  int32_t off;  /* element offset of the entry's blocks in psi.gtab (multiple of 8) */
+  int16_t MW;   /* window half-width in output columns, a multiple of 8 */
+  int16_t KB;   /* 16-column steps of one tile block: ceil((TQ + 2 MW) / 16) */
+  int16_t nch;  /* 64-column chunks: ceil(KB / 4) */
+  int16_t pad;
+} disco_grp_ent;
+
 /* psi: sizes set by disco_psi_plan, device pointers (into the caller's psi
    buffer) set by disco_build_psi_kpacked.  Read-only after the build.
    Index structures are int32; values fp32. */
@@ -106,7 +117,10 @@ typedef struct {
   int64_t nruns;    /* (ho, hi) segments */
   int64_t nhval;    /* rows of hval */
   int64_t nftab;    /* elements of ftab */
-  int64_t nbtab;    /* elements of btab */
+  int32_t ngrp;     /* input-row groups with transpose tables (0 if s > 2) */
+  int32_t grp_max;  /* most entries of one group */
+  int64_t ngrp_ent; /* entries summed over groups */
+  int64_t ngtab;    /* elements of gtab */
   size_t bytes;     /* device bytes disco_build_psi_kpacked needs */
   /* Union ("kpacked") layout, shared across k (§kpacked layout):
      neighbours of output row ho (for output longitude 0) are entries
@@ -130,15 +144,24 @@ typedef struct {
   /* bf16 tables of each run for the tensor-core tiles (values rounded from val).
      Forward table of run r: K rows of TLf = roundup8(len + 16) elements at
      ftab + ftab_off[r]; row k holds psi_k(delta) at index 8 + delta - dlo for
-     the run's offsets dlo..dhi and zeros elsewhere.
-     Transpose (polyphase) table of run r: K*s rows of TLb = roundup8(EH - EL + 17)
-     elements at btab + btab_off[r], EH = floor(dhi/s), EL = ceil((dlo - s + 1)/s);
-     row k*s + p holds psi_k(s*e + p) at index 8 + EH - e (offsets descending)
-     and zeros elsewhere. */
+     the run's offsets dlo..dhi and zeros elsewhere. */
   int32_t* ftab_off;    /* [nruns + 1], multiples of 8 */
   uint16_t* ftab;       /* [nftab] */
-  int32_t* btab_off;    /* [nruns + 1], multiples of 8 */
-  uint16_t* btab;       /* [nbtab] */
+  /* Transpose tables by input-row group, for s <= 2 (the tensor-core
+     transpose tiles): group z holds input rows 8z .. 8z+7; with TQ = 32 / s,
+     grp_ptr[z] .. grp_ptr[z+1]-1 are its entries, one per output row ho that
+     one of its rows reads, ho ascending, with
+       MW  = max over the group's runs (ho, hi) of max(EH, -EL) rounded up to 8,
+             EH = floor(dhi/s), EL = ceil((dlo - s + 1)/s),
+       KB  = ceil((TQ + 2 MW) / 16), nch = ceil(KB / 4).
+     Block (k, c), c < nch, of an entry is 8*s*CW bf16 values at
+     gtab + off + (k*nch + c) * 8*s*CW, CW = roundup8(63 + TQ); element
+     [r][p][y] is psi_k of run (ho, 8z + r) at offset s*e + p,
+     e = MW + TQ - 1 - 64c - y, when that run exists and holds that offset,
+     else 0. */
+  int32_t* grp_ptr;     /* [ngrp + 1] */
+  disco_grp_ent* grp;   /* [ngrp_ent] */
+  uint16_t* gtab;       /* [ngtab] */
 } disco_psi;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -259,7 +282,8 @@ DISCO_API int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const voi
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,
    bit 2 = one of the tensor-core forward contraction timed out,
-   bit 3 = one of the tensor-core transpose contraction timed out; a
+   bit 3 = one of the tensor-core transpose contraction timed out or met an
+   input-row group reading more output rows than it can hold; a
    kernel that times out stops issuing work, frees its tensor memory and
    returns, leaving its outputs incomplete).  clear != 0 resets the word. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);

@@ -55,7 +55,7 @@ class disco_run(ctypes.Structure):
 
 
 _PSI_ARRAYS = ["row_ptr", "idx", "val", "csr_row_ptr", "csr_col", "csr_val", "run_ptr", "runs",
-               "trun_ptr", "truns", "hval", "row_order", "ftab_off", "ftab", "btab_off", "btab"]
+               "trun_ptr", "truns", "hval", "row_order", "ftab_off", "ftab", "grp_ptr", "grp", "gtab"]
 
 
 class disco_psi(ctypes.Structure):
@@ -63,7 +63,8 @@ class disco_psi(ctypes.Structure):
                 ("K", ctypes.c_int32), ("K_pad", ctypes.c_int32), ("s", ctypes.c_int32),
                 ("max_row", ctypes.c_int32), ("nnz", ctypes.c_int64), ("nnz_csr", ctypes.c_int64),
                 ("nruns", ctypes.c_int64), ("nhval", ctypes.c_int64), ("nftab", ctypes.c_int64),
-                ("nbtab", ctypes.c_int64), ("bytes", ctypes.c_size_t)] + \
+                ("ngrp", ctypes.c_int32), ("grp_max", ctypes.c_int32), ("ngrp_ent", ctypes.c_int64),
+                ("ngtab", ctypes.c_int64), ("bytes", ctypes.c_size_t)] + \
                [(n, ctypes.c_void_p) for n in _PSI_ARRAYS]
 
 
@@ -249,7 +250,7 @@ class Psi:
     _DT = {"row_ptr": "int32", "idx": "int32", "val": "float32", "csr_row_ptr": "int32",
            "csr_col": "int32", "csr_val": "float32", "run_ptr": "int32", "runs": "int32",
            "trun_ptr": "int32", "truns": "int32", "hval": "float32", "row_order": "int32",
-           "ftab_off": "int32", "ftab": "int16", "btab_off": "int32", "btab": "int16"}
+           "ftab_off": "int32", "ftab": "int16", "grp_ptr": "int32", "grp": "int32", "gtab": "int16"}
 
     def __init__(self, grid_in, grid_out, kind: int, n_radial: int, cutoff: float, stream=None):
         import torch
@@ -269,7 +270,7 @@ class Psi:
                 "csr_val": (c.nnz_csr,), "run_ptr": (Hout + 1,), "runs": (c.nruns, 8),
                 "trun_ptr": (Hin + 1,), "truns": (c.nruns,), "hval": (c.nhval, c.K_pad),
                 "row_order": (Hout,), "ftab_off": (c.nruns + 1,), "ftab": (c.nftab,),
-                "btab_off": (c.nruns + 1,), "btab": (c.nbtab,)}
+                "grp_ptr": (c.ngrp + 1,), "grp": (c.ngrp_ent, 4), "gtab": (c.ngtab,)}
 
     def tensor(self, name: str):
         """Device view of one psi array (for inspection and tests)."""

@@ -3,29 +3,42 @@
 // DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
 // ("backward: CSR transpose contraction (B,C,K,H,W) -> inp") and §Backward
 // direction (gather direction, each input pixel accumulates from its
-// neighbourhood, no atomics; this kernel owns its output rows outright).
+// neighbourhood, no atomics; every output element has exactly one owner).
 //
-// Polyphase form: with input column j = S q + p and offset delta = S e + p,
+// Polyphase form: with input column j = s q + p and offset delta = s e + p,
 //
-//   gx[bc, hi, S q + p] = sum_{ho} sum_k sum_e psi_k^{(ho,hi)}(S e + p) G[bc, k, ho, q - e].
+//   gx[bc, hi, s q + p] = sum_{ho} sum_k sum_e psi_k^{(ho,hi)}(s e + p) G[bc, k, ho, q - e].
 //
-// For a tile of TQ decimated positions q = qb + t and a window of G columns
-// w = qb - MW + i, this is, per (ho, k), an MMA
+// A tile owns 128 channels, a group of 8 input rows hi0 .. hi0+7 (they share
+// most of their output-row neighbourhood, so each G row is loaded once for
+// all eight) and 2 blocks of TQ = 32/s decimated positions (2 x 32 input
+// columns).  For one output row ho of the group (window half-width MW) and one
+// k, block b of the tile is the MMA
 //
-//   D[bc, (r, t, p)] += sum_i G[bc, k, ho, qb - MW + i] * T[(r, t, p), i],
-//   T[(r, t, p), i] = psi_k^{(ho, hi0 + r)}(S (t - i + MW) + p),
+//   D_b[bc, (r, t, p)] += sum_i G[bc, k, ho, qb + b TQ - MW + i] * T[(r, t, p), i],
+//   T[(r, t, p), i] = psi_k^{(ho, hi0 + r)}(s (t - i + MW) + p),
 //
-// with M = 128 channels, N = 4 rows x S phases x TQ = 256 (ordered so that
-// the N columns of row r are its output columns in order), and the window i
-// as the K extent.  One CTA owns 4 consecutive input rows (they share most
-// of their output-row neighbourhood, so every G window is loaded once for
-// all four), 128 channels and 2 column tiles (TMEM: 2 x 256 columns).
-// Per (ho, k, 64-column chunk) one pipeline stage holds
-//   A  the G window, by TMA (8-column boxes of 128 channels, wrapped column),
-//   tables  the 4 runs' bf16 polyphase tables of psi (bulk copies),
-//   B  T built from the tables by 6 warps.
-// Roles: warp 0 TMA/bulk producer and TMEM owner, warp 1 MMA issuer, warps
-// 2-7 builders; all 8 warps run the epilogue.  All mbarrier waits are bounded.
+// M = 128 channels, N = 8 rows x 32 columns = 256, K = the window, 16 columns
+// per step.  T does not depend on the block, so one T serves both blocks (the
+// second block reads the G window TQ columns further on).  The T values come
+// from the psi tables by input-row group (disco_psi.gtab), laid out so that a
+// 64-column chunk of T is one contiguous block per (ho, k, chunk): every
+// builder thread reads 8 consecutive values with no bounds logic.
+//
+// Operands are K-major in the 128-byte swizzled layout: the G window arrives
+// by TMA in boxes of 64 columns x 128 channels (a box that would cross the
+// longitude seam is fetched instead as 8 wrapped 8-column boxes in the
+// unswizzled layout and read with that layout's descriptor); T is written in
+// the same swizzled layout by the builder warps.
+//
+// Persistent kernel: one CTA per SM walks the tiles round-robin, polar row
+// groups first; the pipeline runs across tile boundaries:
+//   warp 0      producer: per tile the group's entry list (bulk copy), per item
+//               (ho, k, chunk) the psi block (bulk copy) and 1-2 G boxes (TMA);
+//   warp 1      MMA issuer (one thread);
+//   warps 2-7   build T;
+//   warps 8-11  epilogue: tcgen05.ld, bf16, 16-byte row stores.
+// All mbarrier waits are bounded (time-out -> status flag, abort).
 
 #include <cudaTypedefs.h>
 
@@ -38,15 +51,16 @@ __device__ int g_btc_status = 0;
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBuilderThreads = 192;
-constexpr int kNR = 4;                      // input rows per CTA
-constexpr int kNT = 2;                      // column tiles per CTA
-constexpr int kN = 256;                     // MMA N = kNR * S * TQ
-constexpr int kCK = 4;                      // K steps per chunk
-constexpr int kChunkW = kCK * 16;           // 64 window columns
+constexpr int kThreads = 384;
+constexpr int kBuilderThreads = 192;        // warps 2-7
+constexpr int kEpiThreads = 128;            // warps 8-11
+constexpr int kN = 256;                     // MMA N = 8 rows x 32 columns
+constexpr int kNT = 2;                      // column blocks per tile
 constexpr int kStages = 3;
-constexpr uint32_t kGroupBytes = 128 * 16;  // one TMA box: 128 channels x 8 columns
+constexpr int kMaxEnt = 128;                // entries (output rows) of one group
+constexpr uint32_t kBoxBytes = 128 * 128;   // 128 channels x 64 columns bf16
+constexpr uint32_t kNarrowBytes = 128 * 16; // 128 channels x 8 columns
+constexpr uint32_t kTBytes = kN * 128;      // T chunk: 256 rows x 64 columns
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusBtcTimeout = 8;
 
@@ -56,7 +70,6 @@ __device__ __forceinline__ int wrapc(int c, int W) {
   int r = c % W;
   return r < 0 ? r + W : r;
 }
-__device__ __forceinline__ int fdiv(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 __device__ __forceinline__ bool all_named(bool pred, int id, int n) {
   uint32_t r;
@@ -92,105 +105,80 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
 
 struct BtcArgs {
   __nv_bfloat16* gx;  // [BC][Hin][Win]
-  const disco_run* runs;
-  const int32_t* trun_ptr;
-  const int32_t* truns;
-  const int32_t* btab_off;
-  const uint16_t* btab;
+  const int32_t* grp_ptr;
+  const disco_grp_ent* grp;
+  const uint16_t* gtab;
   int BC, Hin, Win, Hout, Wout, K;
-  int TLB;  // table row capacity (>= every run's row length, multiple of 8)
+  int ntx, nty, ntz;  // tiles along columns, channel blocks, row groups
 };
-
-// per-run polyphase geometry
-struct RunP {
-  int EH;   // floor(dhi / S)
-  int E;    // max |e| over the run
-  int TL;   // table row length
-};
-
-template <int S>
-__device__ __forceinline__ RunP run_p(const disco_run& r, int Win) {
-  const int dlo = (r.len == Win) ? -(Win / 2) : -r.npair;
-  const int dhi = dlo + r.len - 1;
-  RunP g;
-  g.EH = fdiv(dhi, S);
-  const int EL = -fdiv(-(dlo - S + 1), S);  // ceil((dlo - S + 1) / S)
-  g.E = max(g.EH, -EL);
-  g.TL = (g.EH - EL + 1 + 16 + 7) & ~7;
-  return g;
-}
-
-// run of (ho, hi) or -1, from hi's transposed list (ascending ho, contiguous)
-__device__ __forceinline__ int find_run(const BtcArgs& a, int hi, int ho) {
-  const int b = a.trun_ptr[hi], e = a.trun_ptr[hi + 1];
-  if (b == e) return -1;
-  const int first = a.runs[a.truns[b]].ho;
-  const int pos = b + (ho - first);
-  if (pos >= b && pos < e && a.runs[a.truns[pos]].ho == ho) return a.truns[pos];
-  for (int i = b; i < e; ++i)
-    if (a.runs[a.truns[i]].ho == ho) return a.truns[i];
-  return -1;
-}
 
 template <int S>
 struct BCfg {
-  static constexpr int TQ = kN / (kNR * S);                         // decimated positions per tile
-  static constexpr int AG = (TQ * (kNT - 1) + kChunkW) / 8;        // A groups per stage
-  static constexpr uint32_t kABytes = AG * kGroupBytes;
-  static constexpr uint32_t kBBytes = kN * kChunkW * 2;
-  static constexpr uint32_t kSBOB = (kChunkW / 8) * 128;            // 1024
-  __host__ __device__ static uint32_t tab_bytes(int TLB) { return (uint32_t)kNR * S * TLB * 2; }
-  // stages start on 1 KB boundaries (TMA destinations need 128-byte alignment)
-  __host__ __device__ static uint32_t stage_bytes(int TLB) {
-    return (kABytes + kBBytes + tab_bytes(TLB) + 1023) & ~1023u;
-  }
-  __host__ __device__ static size_t smem(int TLB) { return (size_t)kStages * stage_bytes(TLB) + 256; }
+  static constexpr int TQ = grp_tq(S);
+  static constexpr int CW = grp_cw(S);
+  static constexpr uint32_t kTabBytes = (uint32_t)grp_block(S) * 2;
+  static constexpr uint32_t kTabSlot = (kTabBytes + 1023) & ~1023u;
+  // stage: 2 G box slots | T chunk | psi block
+  static constexpr uint32_t kStageBytes = 2 * kBoxBytes + kTBytes + kTabSlot;
+  static constexpr uint32_t kInfoBytes = 2 * kMaxEnt * sizeof(disco_grp_ent);
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kInfoBytes + 256 + 1024;
 };
 
-// ho range of the CTA: union of the rows' neighbourhoods
-__device__ __forceinline__ void ho_range(const BtcArgs& a, int hi0, int* lo, int* hi_) {
-  int l = 1 << 30, h = -1;
-  for (int r = 0; r < kNR; ++r) {
-    const int hi = hi0 + r;
-    if (hi >= a.Hin) break;
-    const int b = a.trun_ptr[hi], e = a.trun_ptr[hi + 1];
-    if (b == e) continue;
-    l = min(l, a.runs[a.truns[b]].ho);
-    h = max(h, a.runs[a.truns[e - 1]].ho);
-  }
-  *lo = l;
-  *hi_ = h;
+// the z-th row group in processing order: poles first, then inwards
+__device__ __forceinline__ int row_group(int z, int nz) { return (z & 1) ? nz - 1 - (z >> 1) : (z >> 1); }
+
+template <int S>
+__device__ __forceinline__ void tile_coords(const BtcArgs& a, int tile, int* qb, int* bc0, int* zg) {
+  const int x = tile % a.ntx;
+  const int rest = tile / a.ntx;
+  const int y = rest % a.nty;
+  const int z = rest / a.nty;
+  *qb = x * (kNT * BCfg<S>::TQ);
+  *bc0 = y * 128;
+  *zg = row_group(z, a.ntz);
 }
+
+// a G box that would cross the longitude seam is fetched as 8 narrow boxes
+__device__ __forceinline__ bool box_is_narrow(int col0, int Wout) { return wrapc(col0, Wout) + 64 > Wout; }
 
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc_kernel(const __grid_constant__ CUtensorMap gmap, const BtcArgs a) {
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap gwide, const __grid_constant__ CUtensorMap gnarrow,
+                  const BtcArgs a) {
   using Cfg = BCfg<S>;
-  constexpr int TQ = Cfg::TQ;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t stage_bytes = Cfg::stage_bytes(a.TLB);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
-  uint64_t* fullA = bars;
-  uint64_t* fullT = bars + kStages;
-  uint64_t* fullB = bars + 2 * kStages;
-  uint64_t* empty = bars + 3 * kStages;
-  uint64_t* done = bars + 4 * kStages;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4 * kStages + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kStages + 2);
+  constexpr int TQ = Cfg::TQ, CW = Cfg::CW;
+  constexpr int kStep1 = TQ / 16;  // K steps between the two blocks' windows
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  disco_grp_ent* infos = reinterpret_cast<disco_grp_ent*>(smem + kStages * Cfg::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes + Cfg::kInfoBytes);
+  uint64_t* fullA = bars;                         // [kStages] G boxes + psi block landed
+  uint64_t* fullB = bars + kStages;               // [kStages] T built (192 arrivals)
+  uint64_t* empty = bars + 2 * kStages;           // [kStages] MMAs of the stage done (commit)
+  uint64_t* info_full = bars + 3 * kStages;       // [2] entry list landed
+  uint64_t* info_empty = bars + 3 * kStages + 2;  // [2] entry list released by all readers
+  uint64_t* acc_full = bars + 3 * kStages + 4;    // all MMAs of a tile done (commit)
+  uint64_t* tmem_empty = bars + 3 * kStages + 5;  // epilogue read TMEM out (128 arrivals)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 6);
+  int32_t* info_cnt = reinterpret_cast<int32_t*>(bars + 3 * kStages + 7);  // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kStages + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qb = blockIdx.x * (kNT * TQ);
-  const int bc0 = blockIdx.y * 128;
-  const int hi0 = blockIdx.z * kNR;
+  const int ntiles = a.ntx * a.nty * a.ntz;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&fullA[s], 1);
-      mbar_init(&fullT[s], 1);
       mbar_init(&fullB[s], kBuilderThreads);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&info_full[b], 1);
+      mbar_init(&info_empty[b], 1 + kBuilderThreads + kEpiThreads);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(tmem_empty, kEpiThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -203,68 +191,72 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  int ho_lo, ho_hi;
-  ho_range(a, hi0, &ho_lo, &ho_hi);
-
-  // the per-ho window half-width MW and K steps KS, shared by all roles
-  auto ho_geom = [&](int ho, int* rid, RunP* rp, int* MW, int* KS) {
-    int E = 0;
-    for (int r = 0; r < kNR; ++r) {
-      rid[r] = (hi0 + r < a.Hin) ? find_run(a, hi0 + r, ho) : -1;
-      if (rid[r] >= 0) {
-        rp[r] = run_p<S>(a.runs[rid[r]], a.Win);
-        E = max(E, rp[r].E);
-      }
-    }
-    *MW = (E + 7) & ~7;
-    *KS = (TQ + 2 * *MW + 15) >> 4;
-  };
-
   if (warp == 0) {
-    // ---------------------------------------------- TMA / bulk producer --
+    // ---------------------------------------------------------- producer --
     if (lane == 0) {
-      int i = 0;
-      bool aborted = false;
-      for (int ho = ho_lo; ho <= ho_hi && !aborted; ++ho) {
-        int rid[kNR];
-        RunP rp[kNR];
-        int MW, KS;
-        ho_geom(ho, rid, rp, &MW, &KS);
-        for (int k = 0; k < a.K && !aborted; ++k)
-          for (int c = 0; c * kCK < KS; ++c, ++i) {
-            const int s = i % kStages;
-            if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) ||
-                *abort_flag) {
-              btc_flag(kStatusBtcTimeout);
-              *abort_flag = 1;
-              aborted = true;
-              break;
-            }
-            uint8_t* st = smem + (size_t)s * stage_bytes;
-            uint8_t* tab = st + Cfg::kABytes + Cfg::kBBytes;
-            uint32_t tbytes = 0;
-            for (int r = 0; r < kNR; ++r)
-              if (rid[r] >= 0) tbytes += S * rp[r].TL * 2;
-            mbar_expect_tx(&fullT[s], tbytes);
-            for (int r = 0; r < kNR; ++r)
-              if (rid[r] >= 0)
-                bulk_copy(tab + (size_t)r * S * a.TLB * 2,
-                          a.btab + a.btab_off[rid[r]] + (size_t)k * S * rp[r].TL, S * rp[r].TL * 2,
-                          &fullT[s]);
-            const int nks = min(kCK, KS - c * kCK);
-            const int ng = (TQ * (kNT - 1) + 16 * nks) / 8;
-            mbar_expect_tx(&fullA[s], ng * kGroupBytes);
-            const int w0 = qb - MW + c * kChunkW;
-            for (int gi = 0; gi < ng; ++gi)
-              tma_load_3d(st + gi * kGroupBytes, &gmap, wrapc(w0 + 8 * gi, a.Wout), k * a.Hout + ho,
-                          bc0, &fullA[s]);
+      int i = 0, tl = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
+        int qb, bc0, zg;
+        tile_coords<S>(a, tile, &qb, &bc0, &zg);
+        const int b = tl & 1;
+        if ((tl >= 2 && !mbar_wait(&info_empty[b], ((tl >> 1) - 1) & 1, kWaitLimit)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const int e0 = a.grp_ptr[zg];
+        const int ne = min(a.grp_ptr[zg + 1] - e0, kMaxEnt);
+        info_cnt[b] = ne;
+        disco_grp_ent* info = infos + b * kMaxEnt;
+        if (ne > 0) {
+          mbar_expect_tx(&info_full[b], ne * (uint32_t)sizeof(disco_grp_ent));
+          bulk_copy(info, a.grp + e0, ne * (uint32_t)sizeof(disco_grp_ent), &info_full[b]);
+          if (!mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit)) {
+            ok = false;
+            break;
           }
+        } else {
+          mbar_arrive(&info_full[b]);
+        }
+        for (int j = 0; j < ne && ok; ++j) {
+          const disco_grp_ent en = info[j];
+          for (int k = 0; k < a.K && ok; ++k)
+            for (int c = 0; c < en.nch; ++c, ++i) {
+              const int s = i % kStages;
+              if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) ||
+                  *abort_flag) {
+                ok = false;
+                break;
+              }
+              uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
+              const int nsteps = min(4, (int)en.KB - 4 * c);
+              const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
+              mbar_expect_tx(&fullA[s], nbox * kBoxBytes + Cfg::kTabBytes);
+              bulk_copy(st + 2 * kBoxBytes + kTBytes,
+                        a.gtab + en.off + (size_t)(k * en.nch + c) * grp_block(S), Cfg::kTabBytes,
+                        &fullA[s]);
+              const int row = k * a.Hout + en.ho;
+              for (int bb = 0; bb < nbox; ++bb) {
+                const int col0 = qb - en.MW + 64 * (c + bb);
+                uint8_t* slot = st + bb * kBoxBytes;
+                if (!box_is_narrow(col0, a.Wout)) {
+                  tma_load_3d(slot, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
+                } else {
+                  for (int g = 0; g < 8; ++g)
+                    tma_load_3d(slot + g * kNarrowBytes, &gnarrow, wrapc(col0 + 8 * g, a.Wout), row, bc0,
+                                &fullA[s]);
+                }
+              }
+            }
+        }
       }
-      if (aborted) {
+      if (!ok) {
+        btc_flag(kStatusBtcTimeout);
+        *abort_flag = 1;
+        // let the copies in flight land before the CTA exits
         for (int back = 1; back <= kStages && i - back >= 0; ++back) {
           const int li = i - back;
           mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
-          mbar_wait(&fullT[li % kStages], (li / kStages) & 1, kWaitLimit);
         }
       }
     }
@@ -272,124 +264,148 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kN);
-      int i = 0;
+      int i = 0, tl = 0;
       bool ok = true;
-      for (int ho = ho_lo; ho <= ho_hi && ok; ++ho) {
-        int rid[kNR];
-        RunP rp[kNR];
-        int MW, KS;
-        ho_geom(ho, rid, rp, &MW, &KS);
-        for (int k = 0; k < a.K && ok; ++k)
-          for (int c = 0; c * kCK < KS; ++c, ++i) {
-            const int s = i % kStages;
-            const uint32_t ph = (i / kStages) & 1;
-            if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) ||
-                *abort_flag) {
-              btc_flag(kStatusBtcTimeout);
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int nks = min(kCK, KS - c * kCK);
-            const uint32_t abase = smem_u32(smem + (size_t)s * stage_bytes);
-            const uint32_t bbase = abase + Cfg::kABytes;
-            for (int j = 0; j < kNT; ++j)
-              for (int ks = 0; ks < nks; ++ks) {
-                const uint64_t ad = smem_desc(abase + (uint32_t)(j * TQ / 8 + 2 * ks) * kGroupBytes,
-                                              kGroupBytes, 128);
-                const uint64_t bd = smem_desc(bbase + ks * 256, 128, Cfg::kSBOB);
-                umma_bf16(tmem + j * kN, ad, bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
+        int qb, bc0, zg;
+        tile_coords<S>(a, tile, &qb, &bc0, &zg);
+        const int b = tl & 1;
+        if (!mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) ||
+            (tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int ne = info_cnt[b];
+        const disco_grp_ent* info = infos + b * kMaxEnt;
+        bool first = true;
+        for (int j = 0; j < ne && ok; ++j) {
+          const disco_grp_ent en = info[j];
+          for (int k = 0; k < a.K && ok; ++k)
+            for (int c = 0; c < en.nch; ++c, ++i) {
+              const int s = i % kStages;
+              const uint32_t ph = (i / kStages) & 1;
+              if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) ||
+                  *abort_flag) {
+                ok = false;
+                break;
               }
-            umma_commit(&empty[s]);
+              tc_fence_after();
+              const uint32_t sbase = smem_u32(smem + (size_t)s * Cfg::kStageBytes);
+              const uint32_t tbase = sbase + 2 * kBoxBytes;
+              const bool narrow0 = box_is_narrow(qb - en.MW + 64 * c, a.Wout);
+              const bool narrow1 = box_is_narrow(qb - en.MW + 64 * (c + 1), a.Wout);
+              const int nsteps = min(4, (int)en.KB - 4 * c);
+              for (int t = 0; t < nsteps; ++t) {
+                const uint64_t bd = smem_desc_sw128(tbase + 32 * t);
+                for (int blk = 0; blk < kNT; ++blk) {
+                  const int as = t + blk * kStep1;  // K step within the chunk's boxes
+                  const int bb = as >> 2, ka = as & 3;
+                  const uint32_t slot = sbase + bb * kBoxBytes;
+                  const uint64_t ad = (bb ? narrow1 : narrow0)
+                                          ? smem_desc(slot + ka * 2 * kNarrowBytes, kNarrowBytes, 128)
+                                          : smem_desc_sw128(slot + 32 * ka);
+                  umma_bf16(tmem + blk * kN, ad, bd, idesc, (first && t == 0) ? 0u : 1u);
+                }
+              }
+              first = false;
+              umma_commit(&empty[s]);
+            }
+        }
+        if (!ok) break;
+        mbar_arrive(&info_empty[b]);
+        // a tile without entries leaves the accumulators unwritten: the epilogue stores zeros
+        umma_commit(acc_full);
+      }
+      if (!ok) {
+        btc_flag(kStatusBtcTimeout);
+        *abort_flag = 1;
+        if (i > 0)  // let the MMAs in flight finish before TMEM is freed
+          mbar_wait(&empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, kWaitLimit);
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------- T builders (6 warps) --
+    const int btid = tid - 64;
+    int i = 0, tl = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      {
+        const bool mine = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) && !*abort_flag;
+        ok = all_named(mine, 1, kBuilderThreads);
+        if (!ok) break;
+      }
+      const int ne = info_cnt[b];
+      const disco_grp_ent* info = infos + b * kMaxEnt;
+      for (int j = 0; j < ne && ok; ++j) {
+        const int KB = info[j].KB, nch = info[j].nch;
+        for (int k = 0; k < a.K && ok; ++k)
+          for (int c = 0; c < nch; ++c, ++i) {
+            const int s = i % kStages;
+            // fullA(i) is issued only after the MMAs of the stage's previous item completed
+            const bool mine = mbar_wait(&fullA[s], (i / kStages) & 1, kWaitLimit) && !*abort_flag;
+            ok = all_named(mine, 1, kBuilderThreads);
+            if (!ok) break;
+            uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
+            uint8_t* T = st + 2 * kBoxBytes;
+            const uint16_t* tab = reinterpret_cast<const uint16_t*>(st + 2 * kBoxBytes + kTBytes);
+            const int nq = 2 * min(4, KB - 4 * c);  // 16-byte chunks per T row
+            for (int idx = btid; idx < kN * nq; idx += kBuilderThreads) {
+              const int n = idx & (kN - 1), q8 = idx >> 8;
+              const int r = n >> 5, rem = n & 31;
+              const int t = rem / S, p = rem - t * S;
+              const uint16_t* src = tab + (r * S + p) * CW + 8 * q8 - t + TQ - 1;
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) w[e] = (uint32_t)src[2 * e] | ((uint32_t)src[2 * e + 1] << 16);
+              *reinterpret_cast<uint4*>(T + n * 128 + ((q8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&fullB[s]);
           }
       }
-      umma_commit(done);
+      if (!ok) break;
+      mbar_arrive(&info_empty[b]);
+    }
+    if (!ok) {
+      btc_flag(kStatusBtcTimeout);
+      *abort_flag = 1;
     }
   } else {
-    // ------------------------------------------------- B builders (6 warps) --
-    const int btid = tid - 64;
-    int i = 0;
-    bool ok = true;
-    for (int ho = ho_lo; ho <= ho_hi && ok; ++ho) {
-      int rid[kNR];
-      RunP rp[kNR];
-      int MW, KS;
-      ho_geom(ho, rid, rp, &MW, &KS);
-      for (int k = 0; k < a.K && ok; ++k)
-        for (int c = 0; c * kCK < KS; ++c, ++i) {
-          const int s = i % kStages;
-          const uint32_t ph = (i / kStages) & 1;
-          bool mine = true;
-          if (i >= kStages) mine = mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit);
-          mine = mine && mbar_wait(&fullT[s], ph, kWaitLimit) && !*abort_flag;
-          if (!mine) {
-            btc_flag(kStatusBtcTimeout);
-            *abort_flag = 1;
-          }
-          ok = all_named(mine, 1, kBuilderThreads);
-          if (!ok) break;
-          uint8_t* st = smem + (size_t)s * stage_bytes;
-          uint8_t* sB = st + Cfg::kABytes;
-          const uint16_t* tab = reinterpret_cast<const uint16_t*>(st + Cfg::kABytes + Cfg::kBBytes);
-          const int nks = min(kCK, KS - c * kCK);
-          const int ngrp = 2 * nks;
-          for (int idx = btid; idx < kN * ngrp; idx += kBuilderThreads) {
-            const int n = idx % kN, gi = idx / kN;
-            const int r = n / (S * TQ), rem = n - r * (S * TQ);
-            const int t = rem / S, p = rem - t * S;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if (rid[r] >= 0) {
-              // table index of window column c*64 + 8*gi + j is x0 + j
-              const int TL = rp[r].TL;
-              const int x0 = 8 + rp[r].EH - MW - t + c * kChunkW + 8 * gi;
-              const uint16_t* row = tab + (size_t)r * S * a.TLB + (size_t)p * TL;
-              if (x0 + 7 >= 0 && x0 < TL) {
-                uint16_t v[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const int x = x0 + j;
-                  v[j] = (x >= 0 && x < TL) ? row[x] : (uint16_t)0;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) w[j] = (uint32_t)v[2 * j] | ((uint32_t)v[2 * j + 1] << 16);
-              }
-            }
-            *reinterpret_cast<uint4*>(sB + (n >> 3) * Cfg::kSBOB + gi * 128 + (n & 7) * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          fence_proxy_async_smem();
-          mbar_arrive(&fullB[s]);
-        }
-    }
-  }
-
-  // ----------------------------------------------------- epilogue (8 warps) --
-  {
-    bool fin = mbar_wait(done, 0, kWaitLimit);
-    fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
-    const bool any = ho_lo <= ho_hi;
-    if (!fin) {
-      if (lane == 0) btc_flag(kStatusBtcTimeout);
-    } else {
+    // ----------------------------------------------- epilogue (warps 8-11) --
+    const int q = warp & 3;
+    int tl = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      bool fin = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) && mbar_wait(acc_full, tl & 1, kWaitLimit);
+      fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
+      if (!fin) {
+        if (lane == 0) btc_flag(kStatusBtcTimeout);
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
-      const int q = warp & 3, j = warp >> 2 ? 0 : 1;  // warps 4-7: tile 0, warps 0-3: tile 1
+      int qb, bc0, zg;
+      tile_coords<S>(a, tile, &qb, &bc0, &zg);
+      const int hi0 = zg * kGrpRows;
+      const bool any = info_cnt[b] > 0;
       const int bc = bc0 + q * 32 + lane;
-      for (int r = 0; r < kNR; ++r) {
-        const int hi = hi0 + r;
-        for (int cc = 0; cc < (S * TQ) / 16; ++cc) {
-          float v[16];
-          if (any) {
-            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + j * kN + r * (S * TQ) + cc * 16, v);
-          } else {
+      for (int blk = 0; blk < kNT; ++blk)
+        for (int r = 0; r < kGrpRows; ++r) {
+          const int hi = hi0 + r;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = 0.f;
-          }
-          const int col = S * (qb + j * TQ) + cc * 16;
-          if (hi < a.Hin && bc < a.BC && col < a.Win) {
-            __nv_bfloat16* dst = a.gx + ((size_t)bc * a.Hin + hi) * a.Win + col;
-            const int n = min(16, a.Win - col);
-            if (n == 16) {
+          for (int cc = 0; cc < 2; ++cc) {
+            float v[16];
+            if (any) {
+              tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + blk * kN + r * 32 + cc * 16, v);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = 0.f;
+            }
+            const int col = S * (qb + blk * TQ) + cc * 16;
+            if (hi < a.Hin && bc < a.BC && col < a.Win) {
+              __nv_bfloat16* dst = a.gx + ((size_t)bc * a.Hin + hi) * a.Win + col;
               uint32_t w32[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
@@ -397,13 +413,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 w32[e] = *reinterpret_cast<uint32_t*>(&p2);
               }
               reinterpret_cast<uint4*>(dst)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
-              reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
-            } else {
-              for (int e = 0; e < n; ++e) dst[e] = __float2bfloat16_rn(v[e]);
+              if (col + 16 <= a.Win)  // W_in is a multiple of 8
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
             }
           }
         }
-      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+      mbar_arrive(&info_empty[b]);
     }
   }
   tc_fence_before();
@@ -427,43 +444,61 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_b() {
   return fn;
 }
 
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 1;
+  }
+  return n;
+}
+
+int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw, bool swz) {
+  auto enc = encode_fn_b();
+  if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)a.Wout, (cuuint64_t)a.K * a.Hout, (cuuint64_t)BC};
+  cuuint64_t strides[2] = {(cuuint64_t)a.Wout * 2, (cuuint64_t)a.K * a.Hout * a.Wout * 2};
+  cuuint32_t box[3] = {(cuuint32_t)boxw, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(G), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  return DISCO_OK;
+}
+
 template <int S>
 int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st) {
   using Cfg = BCfg<S>;
   BtcArgs a;
   a.gx = (__nv_bfloat16*)gx;
-  a.runs = psi->runs;
-  a.trun_ptr = psi->trun_ptr;
-  a.truns = psi->truns;
-  a.btab_off = psi->btab_off;
-  a.btab = psi->btab;
+  a.grp_ptr = psi->grp_ptr;
+  a.grp = psi->grp;
+  a.gtab = psi->gtab;
   a.BC = BC;
   a.Hin = psi->grid_in.nlat;
   a.Win = psi->grid_in.nlon;
   a.Hout = psi->grid_out.nlat;
   a.Wout = psi->grid_out.nlon;
   a.K = psi->K;
-  // a run spans at most one ring: EH - EL + 1 <= (W_in - 1 + S)/S + 1
-  a.TLB = ((a.Win - 1 + S) / S + 1 + 1 + 16 + 7) & ~7;
-  const size_t smem = Cfg::smem(a.TLB);
-  if (smem > 227 * 1024) return DISCO_ERR_UNSUPPORTED;
-  auto enc = encode_fn_b();
-  if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  CUtensorMap map;
-  cuuint64_t dims[3] = {(cuuint64_t)a.Wout, (cuuint64_t)a.K * a.Hout, (cuuint64_t)BC};
-  cuuint64_t strides[2] = {(cuuint64_t)a.Wout * 2, (cuuint64_t)a.K * a.Hout * a.Wout * 2};
-  cuuint32_t box[3] = {8, 1, 128};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(G), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  a.ntx = (a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ);
+  a.nty = (BC + 127) / 128;
+  a.ntz = psi->ngrp;
+  CUtensorMap wide, narrow;
+  int stt = encode_g(&wide, G, a, BC, 64, true);
+  if (stt) return stt;
+  if ((stt = encode_g(&narrow, G, a, BC, 8, false))) return stt;
   auto kern = bwd_tc_kernel<S>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) != cudaSuccess)
     return check_launch("disco_bwd (tensor cores) attribute");
-  dim3 grid((a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ), (BC + 127) / 128,
-            (a.Hin + kNR - 1) / kNR);
-  kern<<<grid, kThreads, smem, st>>>(map, a);
+  const long long ntiles = (long long)a.ntx * a.nty * a.ntz;
+  const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(wide, narrow, a);
   return check_launch("disco_bwd (tensor cores)");
 }
 
@@ -481,9 +516,13 @@ cudaError_t btc_status(int32_t* v, bool clear) {
 }
 
 int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st) {
-  if (psi->grid_out.nlon % 8 != 0 || psi->grid_in.nlon % 8 != 0 || (psi->s != 1 && psi->s != 2) ||
-      BC > 65535 * 128 || psi->K > 16 || !psi->btab || !psi->btab_off)
+  const int Win = psi->grid_in.nlon, Wout = psi->grid_out.nlon, Hin = psi->grid_in.nlat;
+  if ((psi->s != 1 && psi->s != 2) || Wout % 8 != 0 || Win % 8 != 0 || Wout < 64 || BC < 1 ||
+      psi->K > 16 || !psi->grp_ptr || !psi->grp || !psi->gtab || psi->ngrp_ent < 1 ||
+      psi->ngrp != (Hin + kGrpRows - 1) / kGrpRows || psi->grp_max > kMaxEnt ||
+      (long long)psi->K * psi->grid_out.nlat > (1 << 30))
     return DISCO_ERR_UNSUPPORTED;
+  static_assert(BCfg<1>::kSmem <= 227 * 1024 && BCfg<2>::kSmem <= 227 * 1024, "shared memory");
   return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st) : launch_btc<2>(psi, G, gx, BC, st);
 }
 

@@ -37,6 +37,15 @@ cudaError_t tc_status(int32_t* v, bool clear);
 int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st);
 cudaError_t btc_status(int32_t* v, bool clear);
 
+// Geometry of the transpose tables by input-row group (disco_psi.grp_ptr):
+// 8 input rows per group, 64-column chunks, TQ = 32 / s decimated output
+// columns per tile block, table rows of CW = roundup8(63 + TQ) elements.
+constexpr int kGrpRows = 8;
+constexpr int kGrpChunk = 64;
+__host__ __device__ constexpr int grp_tq(int s) { return 32 / s; }
+__host__ __device__ constexpr int grp_cw(int s) { return (kGrpChunk - 1 + grp_tq(s) + 7) & ~7; }
+__host__ __device__ constexpr int grp_block(int s) { return kGrpRows * s * grp_cw(s); }
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
 

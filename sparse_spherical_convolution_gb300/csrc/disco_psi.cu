@@ -113,7 +113,7 @@ __device__ __host__ inline int run_len(int m, int W) {
   return 2 * m + 1;
 }
 
-constexpr int kRS = 5;  // per-row totals before the ring counts
+constexpr int kRS = 4;  // per-row totals before the ring counts
 
 // run extent: offsets dlo..dhi (full ring of even width: -W/2 .. W/2 - 1)
 __device__ __host__ inline void run_extent(int m, int W, int* dlo, int* dhi) {
@@ -125,27 +125,32 @@ __device__ __host__ inline int floordiv(int a, int b) { return a >= 0 ? a / b : 
 __device__ __host__ inline int ceildiv(int a, int b) { return -floordiv(-a, b); }
 // table row lengths of a run (elements, multiples of 8)
 __device__ __host__ inline int ftab_len(int m, int W) { return (run_len(m, W) + 16 + 7) & ~7; }
-__device__ __host__ inline int btab_len(int m, int W, int s) {
+// half-width of a run in decimated (output) columns: max(EH, -EL) with
+// EH = floor(dhi / s), EL = ceil((dlo - s + 1) / s)
+__device__ __host__ inline int run_halfwidth(int m, int W, int s) {
   int dlo, dhi;
   run_extent(m, W, &dlo, &dhi);
   const int EH = floordiv(dhi, s), EL = ceildiv(dlo - s + 1, s);
-  return (EH - EL + 1 + 16 + 7) & ~7;
+  return EH > -EL ? EH : -EL;
 }
 
 struct Workspace {
   int32_t* mtab;      // [Hout][Hin]
   int32_t* ringcnt;   // [Hout][Hin][R]
   double* hq;         // [Hout][Hin][R]
-  int32_t* rowsum;    // [Hout][5 + R]: len, runs, hval rows, ftab, btab elements, ring counts
+  int32_t* rowsum;    // [Hout][4 + R]: len, runs, hval rows, ftab elements, ring counts
   int32_t* off;       // [Hout][Hin]: entry offset of the run inside its row
   int32_t* runidx;    // [Hout][Hin]
   int32_t* csroff;    // [Hout][Hin][R]
   int32_t* hofftab;   // [Hout][Hin]
   int32_t* ftofftab;  // [Hout][Hin]: forward table offset of the run
-  int32_t* btofftab;  // [Hout][Hin]: transpose table offset of the run
   double* norm;       // [Hout][R]
   int32_t* tcount;    // [Hin + 1]
+  int32_t* gcnt;      // [ngroups][2]: entries, blocks of each input-row group
+  int32_t* gboff;     // [ngroups]: first block of each group
 };
+
+__host__ __device__ inline int num_groups(const PsiGeom& g) { return (g.Hin + kGrpRows - 1) / kGrpRows; }
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -162,13 +167,14 @@ size_t carve_workspace(const PsiGeom& g, char* base, Workspace* ws) {
   w.hq = (double*)take(HH * g.R * 8);
   w.rowsum = (int32_t*)take((size_t)g.Hout * (kRS + g.R) * 4);
   w.ftofftab = (int32_t*)take(HH * 4);
-  w.btofftab = (int32_t*)take(HH * 4);
   w.off = (int32_t*)take(HH * 4);
   w.runidx = (int32_t*)take(HH * 4);
   w.csroff = (int32_t*)take(HH * g.R * 4);
   w.hofftab = (int32_t*)take(HH * 4);
   w.norm = (double*)take((size_t)g.Hout * g.R * 8);
   w.tcount = (int32_t*)take((size_t)(g.Hin + 1) * 4);
+  w.gcnt = (int32_t*)take((size_t)num_groups(g) * 2 * 4);
+  w.gboff = (int32_t*)take((size_t)num_groups(g) * 4);
   if (ws) *ws = w;
   return o;
 }
@@ -215,8 +221,7 @@ __global__ void count_kernel(PsiGeom g, Workspace ws) {
 __global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
   int ho = blockIdx.x * blockDim.x + threadIdx.x;
   if (ho >= g.Hout) return;
-  int len = 0, runs = 0, hrows = 0, ft = 0, bt = 0, rc[kMaxRad] = {0};
-  const int s = g.Win / g.Wout;
+  int len = 0, runs = 0, hrows = 0, ft = 0, rc[kMaxRad] = {0};
   for (int hi = 0; hi < g.Hin; ++hi) {
     size_t t = (size_t)ho * g.Hin + hi;
     int m = ws.mtab[t];
@@ -225,7 +230,6 @@ __global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
     runs += 1;
     hrows += m + 1;  // pair steps delta = 0 .. m (m = W/2 includes the antipodal step)
     ft += g.K * ftab_len(m, g.Win);
-    bt += g.K * s * btab_len(m, g.Win, s);
     for (int r = 0; r < g.R; ++r) rc[r] += ws.ringcnt[t * g.R + r];
   }
   int32_t* o = ws.rowsum + (size_t)ho * (kRS + g.R);
@@ -233,7 +237,6 @@ __global__ void rowsum_kernel(PsiGeom g, Workspace ws) {
   o[1] = runs;
   o[2] = hrows;
   o[3] = ft;
-  o[4] = bt;
   for (int r = 0; r < g.R; ++r) o[kRS + r] = rc[r];
 }
 
@@ -241,8 +244,11 @@ struct PsiOut {
   int32_t *row_ptr, *idx, *csr_row_ptr, *csr_col, *run_ptr, *trun_ptr, *truns, *row_order;
   float *val, *csr_val, *hval;
   disco_run* runs;
-  int32_t *ftab_off, *btab_off;
-  uint16_t *ftab, *btab;
+  int32_t* ftab_off;
+  uint16_t* ftab;
+  int32_t* grp_ptr;
+  disco_grp_ent* grp;
+  uint16_t* gtab;
 };
 
 __device__ __forceinline__ int ring_of(int kind, int k) { return kind == 1 ? k / 3 : k; }
@@ -277,13 +283,11 @@ __global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   int32_t off = 0, run = p.run_ptr[ho];
   // pair-weight rows: runs are numbered globally in (ho, hi) order, so the
   // hval offset of a run is the running total over all earlier runs.
-  int32_t hoff = 0, foff = 0, boff = 0;
+  int32_t hoff = 0, foff = 0;
   for (int h2 = 0; h2 < ho; ++h2) {
     hoff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 2];
     foff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 3];
-    boff += ws.rowsum[(size_t)h2 * (kRS + g.R) + 4];
   }
-  const int s = g.Win / g.Wout;
   int32_t rc[kMaxRad] = {0};
   double nrm[kMaxRad] = {0};
   for (int hi = 0; hi < g.Hin; ++hi) {
@@ -293,14 +297,12 @@ __global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     ws.runidx[t] = m >= 0 ? run : -1;
     ws.hofftab[t] = hoff;
     ws.ftofftab[t] = foff;
-    ws.btofftab[t] = boff;
     for (int r = 0; r < g.R; ++r) ws.csroff[t * g.R + r] = rc[r];
     if (m < 0) continue;
     off += run_len(m, g.Win);
     run += 1;
     hoff += m + 1;
     foff += g.K * ftab_len(m, g.Win);
-    boff += g.K * s * btab_len(m, g.Win, s);
     for (int r = 0; r < g.R; ++r) {
       rc[r] += ws.ringcnt[t * g.R + r];
       nrm[r] = __dadd_rn(nrm[r], ws.hq[t * g.R + r]);
@@ -394,7 +396,6 @@ __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
 // bf16 tables of each run (forward and polyphase transpose), from val
 __global__ void table_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   const int ho = blockIdx.x;
-  const int s = g.Win / g.Wout;
   for (int hi = blockIdx.y; hi < g.Hin; hi += gridDim.y) {
     const size_t t = (size_t)ho * g.Hin + hi;
     const int m = ws.mtab[t];
@@ -403,39 +404,116 @@ __global__ void table_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     const int e0 = p.row_ptr[ho] + ws.off[t];
     int dlo, dhi;
     run_extent(m, g.Win, &dlo, &dhi);
-    const int tlf = ftab_len(m, g.Win), tlb = btab_len(m, g.Win, s);
-    const int foff = ws.ftofftab[t], boff = ws.btofftab[t];
-    if (threadIdx.x == 0) {
-      p.ftab_off[r] = foff;
-      p.btab_off[r] = boff;
-    }
+    const int tlf = ftab_len(m, g.Win);
+    const int foff = ws.ftofftab[t];
+    if (threadIdx.x == 0) p.ftab_off[r] = foff;
     for (int i = threadIdx.x; i < g.K * tlf; i += blockDim.x) {
       const int k = i / tlf, x = i - k * tlf;
       const int d = dlo + x - 8;
       const float v = (d >= dlo && d <= dhi) ? p.val[(size_t)(e0 + d - dlo) * g.Kp + k] : 0.f;
       p.ftab[foff + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
-    const int EH = floordiv(dhi, s);
-    for (int i = threadIdx.x; i < g.K * s * tlb; i += blockDim.x) {
-      const int row = i / tlb, x = i - row * tlb;
-      const int k = row / s, ph = row - k * s;
-      const int e = EH - (x - 8);
-      const int d = s * e + ph;
-      const float v = (x >= 8 && d >= dlo && d <= dhi) ? p.val[(size_t)(e0 + d - dlo) * g.Kp + k] : 0.f;
-      p.btab[boff + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    }
   }
 }
 
 __global__ void table_tail_kernel(PsiGeom g, Workspace ws, PsiOut p, int32_t nruns) {
   if (blockIdx.x != 0 || threadIdx.x != 0) return;
-  int32_t f = 0, b = 0;
-  for (int ho = 0; ho < g.Hout; ++ho) {
-    f += ws.rowsum[(size_t)ho * (kRS + g.R) + 3];
-    b += ws.rowsum[(size_t)ho * (kRS + g.R) + 4];
-  }
+  int32_t f = 0;
+  for (int ho = 0; ho < g.Hout; ++ho) f += ws.rowsum[(size_t)ho * (kRS + g.R) + 3];
   p.ftab_off[nruns] = f;
-  p.btab_off[nruns] = b;
+}
+
+// ---- transpose tables by input-row group (see disco_psi.grp_ptr) --------
+
+// Walks the output rows that input-row group z reads, calling f(ho, MW, KB, nch).
+template <typename F>
+__device__ void for_group_rows(const PsiGeom& g, const Workspace& ws, int z, F f) {
+  const int s = g.Win / g.Wout, TQ = grp_tq(s);
+  const int h0 = z * kGrpRows, h1 = min(g.Hin, h0 + kGrpRows);
+  for (int ho = 0; ho < g.Hout; ++ho) {
+    int E = -1;
+    for (int hi = h0; hi < h1; ++hi) {
+      const int m = ws.mtab[(size_t)ho * g.Hin + hi];
+      if (m >= 0) E = max(E, run_halfwidth(m, g.Win, s));
+    }
+    if (E < 0) continue;
+    const int MW = (E + 7) & ~7;
+    const int KB = (TQ + 2 * MW + 15) / 16;
+    f(ho, MW, KB, (KB + 3) / 4);
+  }
+}
+
+// One thread per group: entries and table blocks.
+__global__ void gcount_kernel(PsiGeom g, Workspace ws) {
+  const int z = blockIdx.x * blockDim.x + threadIdx.x;
+  if (z >= num_groups(g)) return;
+  int ent = 0, blk = 0;
+  for_group_rows(g, ws, z, [&](int, int, int, int nch) {
+    ++ent;
+    blk += g.K * nch;
+  });
+  ws.gcnt[2 * z] = ent;
+  ws.gcnt[2 * z + 1] = blk;
+}
+
+__global__ void gscan_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int32_t e = 0, b = 0;
+  const int nz = num_groups(g);
+  for (int z = 0; z < nz; ++z) {
+    p.grp_ptr[z] = e;
+    ws.gboff[z] = b;
+    e += ws.gcnt[2 * z];
+    b += ws.gcnt[2 * z + 1];
+  }
+  p.grp_ptr[nz] = e;
+}
+
+__global__ void gent_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  const int z = blockIdx.x * blockDim.x + threadIdx.x;
+  if (z >= num_groups(g)) return;
+  const int blk = grp_block(g.Win / g.Wout);
+  int e = p.grp_ptr[z], b = ws.gboff[z];
+  for_group_rows(g, ws, z, [&](int ho, int MW, int KB, int nch) {
+    disco_grp_ent en;
+    en.ho = ho;
+    en.off = b * blk;
+    en.MW = (int16_t)MW;
+    en.KB = (int16_t)KB;
+    en.nch = (int16_t)nch;
+    en.pad = 0;
+    p.grp[e++] = en;
+    b += g.K * nch;
+  });
+}
+
+// One block per group: every element of the group's table blocks.
+__global__ void gfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
+  const int z = blockIdx.x;
+  const int s = g.Win / g.Wout, TQ = grp_tq(s), CW = grp_cw(s), blk = grp_block(s);
+  for (int j = p.grp_ptr[z]; j < p.grp_ptr[z + 1]; ++j) {
+    const disco_grp_ent en = p.grp[j];
+    const int n = g.K * en.nch * blk;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int bi = i / blk, w = i - bi * blk;  // block (k, c), element (r, ph, y)
+      const int k = bi / en.nch, c = bi - k * en.nch;
+      const int r = w / (s * CW), ph = (w / CW) % s, y = w % CW;
+      const int hi = z * kGrpRows + r;
+      float v = 0.f;
+      if (hi < g.Hin) {
+        const size_t t = (size_t)en.ho * g.Hin + hi;
+        const int m = ws.mtab[t];
+        const int d = s * (en.MW + TQ - 1 - kGrpChunk * c - y) + ph;
+        int dlo, dhi;
+        run_extent(m, g.Win, &dlo, &dhi);
+        if (m >= 0 && d >= dlo && d <= dhi) {
+          const int e0 = p.row_ptr[en.ho] + ws.off[t];
+          v = p.val[(size_t)(e0 + d - dlo) * g.Kp + k];
+        }
+      }
+      p.gtab[(size_t)en.off + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
 }
 
 // transposed run list: count per input row, scan, fill (ho ascending)
@@ -535,8 +613,9 @@ size_t carve_psi(const disco_psi* psi, char* base, PsiOut* out) {
   p.row_order = (int32_t*)take((size_t)Hout * 4);
   p.ftab_off = (int32_t*)take((size_t)(psi->nruns + 1) * 4);
   p.ftab = (uint16_t*)take((size_t)psi->nftab * 2);
-  p.btab_off = (int32_t*)take((size_t)(psi->nruns + 1) * 4);
-  p.btab = (uint16_t*)take((size_t)psi->nbtab * 2);
+  p.grp_ptr = (int32_t*)take((size_t)(psi->ngrp + 1) * 4);
+  p.grp = (disco_grp_ent*)take((size_t)psi->ngrp_ent * sizeof(disco_grp_ent));
+  p.gtab = (uint16_t*)take((size_t)psi->ngtab * 2);
   if (out) *out = p;
   return o;
 }
@@ -580,7 +659,7 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
   cudaError_t ce = cudaMemcpyAsync(rs.data(), ws.rowsum, rs.size() * 4, cudaMemcpyDeviceToHost, s);
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
   if (ce != cudaSuccess) return fail(DISCO_ERR_CUDA, "psi plan copy: %s", cudaGetErrorString(ce));
-  int64_t nnz = 0, nruns = 0, nhval = 0, nnz_csr = 0, nftab = 0, nbtab = 0;
+  int64_t nnz = 0, nruns = 0, nhval = 0, nnz_csr = 0, nftab = 0;
   int32_t max_row = 0;
   for (int ho = 0; ho < g.Hout; ++ho) {
     const int32_t* o = &rs[(size_t)ho * (kRS + g.R)];
@@ -588,12 +667,29 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
     nruns += o[1];
     nhval += o[2];
     nftab += o[3];
-    nbtab += o[4];
     if (o[0] > max_row) max_row = o[0];
     for (int k = 0; k < g.K; ++k) nnz_csr += o[kRS + (g.kind == 1 ? k / 3 : k)];
   }
+  // transpose tables by input-row group (s <= 2 only)
+  const int sdec = g.Win / g.Wout;
+  const int nz = sdec <= 2 ? num_groups(g) : 0;
+  int64_t ngrp_ent = 0, ngtab = 0;
+  int32_t grp_max = 0;
+  if (nz > 0) {
+    gcount_kernel<<<(nz + 127) / 128, 128, 0, s>>>(g, ws);
+    if ((st = check_launch("psi group count"))) return st;
+    std::vector<int32_t> gc((size_t)nz * 2);
+    ce = cudaMemcpyAsync(gc.data(), ws.gcnt, gc.size() * 4, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) return fail(DISCO_ERR_CUDA, "psi plan copy: %s", cudaGetErrorString(ce));
+    for (int z = 0; z < nz; ++z) {
+      ngrp_ent += gc[2 * z];
+      ngtab += (int64_t)gc[2 * z + 1] * grp_block(sdec);
+      if (gc[2 * z] > grp_max) grp_max = gc[2 * z];
+    }
+  }
   if (nnz >= ((int64_t)1 << 31) / 16 || nnz_csr >= ((int64_t)1 << 31) || nftab >= ((int64_t)1 << 31) ||
-      nbtab >= ((int64_t)1 << 31))
+      ngtab >= ((int64_t)1 << 31))
     return fail(DISCO_ERR_UNSUPPORTED, "psi too large for int32 offsets");
   memset(psi, 0, sizeof(*psi));
   psi->grid_in = *grid_in;
@@ -608,7 +704,10 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
   psi->nruns = nruns;
   psi->nhval = nhval;
   psi->nftab = nftab;
-  psi->nbtab = nbtab;
+  psi->ngrp = nz;
+  psi->grp_max = grp_max;
+  psi->ngrp_ent = ngrp_ent;
+  psi->ngtab = ngtab;
   psi->bytes = carve_psi(psi, nullptr, nullptr);
   return DISCO_OK;
 }
@@ -653,6 +752,15 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   if ((st = check_launch("psi tfill"))) return st;
   order_kernel<<<(g.Hout + tb - 1) / tb, tb, 0, s>>>(g, ws, p);
   if ((st = check_launch("psi order"))) return st;
+  if (psi->ngrp > 0) {
+    // the group counts were left in the workspace by disco_psi_plan
+    gscan_kernel<<<1, 1, 0, s>>>(g, ws, p);
+    if ((st = check_launch("psi group scan"))) return st;
+    gent_kernel<<<(psi->ngrp + 127) / 128, 128, 0, s>>>(g, ws, p);
+    if ((st = check_launch("psi group entries"))) return st;
+    gfill_kernel<<<psi->ngrp, 256, 0, s>>>(g, ws, p);
+    if ((st = check_launch("psi group tables"))) return st;
+  }
   psi->row_ptr = p.row_ptr;
   psi->idx = p.idx;
   psi->val = p.val;
@@ -667,7 +775,8 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   psi->row_order = p.row_order;
   psi->ftab_off = p.ftab_off;
   psi->ftab = p.ftab;
-  psi->btab_off = p.btab_off;
-  psi->btab = p.btab;
+  psi->grp_ptr = p.grp_ptr;
+  psi->grp = p.grp;
+  psi->gtab = p.gtab;
   return DISCO_OK;
 }

@@ -103,6 +103,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The same for a K-major operand in the 128-byte swizzled layout (what a TMA
+// box of 64 bf16 columns with CU_TENSOR_MAP_SWIZZLE_128B writes): rows of 128
+// bytes, 16-byte chunk j of row r stored at chunk position j ^ (r % 8), 8-row
+// groups 1024 bytes apart (SBO), tile base 1024-byte aligned; LBO unused (1);
+// layout type 2 = 128-byte swizzle.  The K step k (16 bf16) of a 64-column
+// row starts 32 k bytes after the tile base.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)            // D format: f32

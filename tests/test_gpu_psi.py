@@ -59,7 +59,7 @@ def _close_f32(gpu, ref64):
     assert ulp_diff_f32(gpu[~small], ref32[~small]) <= 1
 
 
-@pytest.mark.parametrize("case", CASES[:2] + CASES[5:], ids=lambda c: f"{c[0]}->{c[1]}")
+@pytest.mark.parametrize("case", CASES[:3] + CASES[5:], ids=lambda c: f"{c[0]}->{c[1]}")
 def test_runs_are_consistent_with_union_layout(lib, case):
     """The kernel-side run table, transposed runs and pair weights describe
     exactly the union layout."""
@@ -112,26 +112,73 @@ def _bf16_bits(v):
 
 
 def _check_tables(psi, runs, val, gi, go):
-    """Forward and polyphase transpose tables hold exactly the bf16-rounded
-    union values at the documented positions and zeros elsewhere."""
+    """Forward tables and the transpose tables by input-row group hold exactly
+    the bf16-rounded union values at the documented positions, zeros elsewhere."""
     K, W, s = psi.c.K, gi[1], gi[1] // go[1]
     ftab, foff = psi.tensor("ftab").cpu().numpy(), psi.tensor("ftab_off").cpu().numpy()
-    btab, boff = psi.tensor("btab").cpu().numpy(), psi.tensor("btab_off").cpu().numpy()
-    assert foff[-1] == psi.c.nftab and boff[-1] == psi.c.nbtab
+    assert foff[-1] == psi.c.nftab
+    ext = {}
     for r, (ho, hi, D, hoff, e0, ln, npair, anti) in enumerate(runs):
         dlo = -(W // 2) if ln == W else -npair
         dhi = dlo + ln - 1
         vb = _bf16_bits(val[e0:e0 + ln, :K])            # [len, K], offsets dlo..dhi
+        ext[(int(ho), int(hi))] = (dlo, dhi, vb)
         TL = (ln + 16 + 7) // 8 * 8
         want = np.zeros((K, TL), np.int16)
         want[:, 8:8 + ln] = vb.T
         assert np.array_equal(ftab[foff[r]:foff[r] + K * TL].reshape(K, TL), want)
-        EH, EL = dhi // s, -((-(dlo - s + 1)) // s)
-        TB = (EH - EL + 1 + 16 + 7) // 8 * 8
-        wantb = np.zeros((K, s, TB), np.int16)
-        for p in range(s):
-            for e in range(EL, EH + 1):
-                d = s * e + p
-                if dlo <= d <= dhi:
-                    wantb[:, p, 8 + EH - e] = vb[d - dlo]
-        assert np.array_equal(btab[boff[r]:boff[r] + K * s * TB].reshape(K, s, TB), wantb)
+    _check_group_tables(psi, ext, gi, go)
+
+
+def _halfwidth(dlo, dhi, s):
+    """max(EH, -EL) with EH = floor(dhi / s), EL = ceil((dlo - s + 1) / s)."""
+    EH = dhi // s
+    EL = -((-(dlo - s + 1)) // s)
+    return max(EH, -EL)
+
+
+def _check_group_tables(psi, ext, gi, go):
+    Hin, W = gi[0], gi[1]
+    s, K = W // go[1], psi.c.K
+    if s > 2:
+        assert psi.c.ngrp == 0
+        return
+    TQ = 32 // s
+    CW = (63 + TQ + 7) // 8 * 8
+    BLK = 8 * s * CW
+    nz = (Hin + 7) // 8
+    assert psi.c.ngrp == nz
+    gptr = psi.tensor("grp_ptr").cpu().numpy()
+    grp = psi.tensor("grp").cpu().numpy()
+    gtab = psi.tensor("gtab").cpu().numpy()
+    assert gptr[0] == 0 and gptr[-1] == psi.c.ngrp_ent
+    assert psi.c.grp_max == int(np.diff(gptr).max())
+    off_next = 0
+    for z in range(nz):
+        rows = range(8 * z, min(Hin, 8 * z + 8))
+        hos = sorted({ho for (ho, hi) in ext if hi in rows})
+        ents = grp[gptr[z]:gptr[z + 1]]
+        assert [int(e[0]) for e in ents] == hos
+        for e in ents:
+            ho, off = int(e[0]), int(e[1])
+            MW, KB, nch = int(e[2]) & 0xFFFF, int(e[2]) >> 16, int(e[3]) & 0xFFFF
+            E = max(_halfwidth(dlo, dhi, s) for (h2, hi), (dlo, dhi, _) in ext.items()
+                    if h2 == ho and hi in rows)
+            assert MW == (E + 7) // 8 * 8
+            assert KB == (TQ + 2 * MW + 15) // 16 and nch == (KB + 3) // 4
+            assert off == off_next
+            off_next += K * nch * BLK
+            want = np.zeros((K, nch, 8, s, CW), np.int16)
+            for r, hi in enumerate(rows):
+                if (ho, hi) not in ext:
+                    continue
+                dlo, dhi, vb = ext[(ho, hi)]
+                for c in range(nch):
+                    for p in range(s):
+                        y = np.arange(CW)
+                        d = s * (MW + TQ - 1 - 64 * c - y) + p
+                        ok = (d >= dlo) & (d <= dhi)
+                        want[:, c, r, p, y[ok]] = vb[d[ok] - dlo].T
+            got = gtab[off:off + K * nch * BLK].reshape(K, nch, 8, s, CW)
+            assert np.array_equal(got, want), (z, ho)
+    assert off_next == psi.c.ngtab
