@@ -197,9 +197,10 @@ DISCO_API int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes
      X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]
                         * x[b,c,hi,(wi + wo*s) mod W_in]
    x: [B, C, H_in, W_in], X: [B, C, K, H_out, W_out], both `dtype`.
-   Supports s in {1, 2}.  bf16 with W_in % 8 == 0 runs on the tensor cores
-   (banded Toeplitz tiles of the run windows, fp32 accumulation in tensor
-   memory); fp32, and bf16 with other widths, run the CUDA-core gather. */
+   Supports s in {1, 2}.  bf16 with W_in % 8 == 0, W_in >= 64 and K <= 9
+   runs on the tensor cores (banded Toeplitz tiles of the run windows, fp32
+   accumulation in tensor memory); fp32, and other bf16 shapes, run the
+   CUDA-core gather. */
 DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
@@ -209,16 +210,18 @@ DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B,
      gx[b,c,hi,wi] = sum_{k,ho,wo} sum_{wi0: (wi0 + wo*s) mod W_in = wi}
                        psi[k,ho,hi,wi0] * G[b,c,k,ho,wo]
    G: [B, C, K, H_out, W_out], gx: [B, C, H_in, W_in], both `dtype`.
-   Each thread block owns whole input rows (latitude-row ownership).  bf16
-   with W_in and W_out multiples of 8 runs on the tensor cores (polyphase
-   Toeplitz tiles, 4 input rows per block sharing each G window); other cases
-   run the CUDA-core gather. */
+   Each output element has one owner (latitude-row ownership, no atomics).
+   bf16 with W_in and W_out multiples of 8, W_out >= 64 and K <= 16 runs on
+   the tensor cores (polyphase Toeplitz tiles, 8 input rows per tile sharing
+   each G window, psi from the tables by input-row group); other cases run the
+   CUDA-core gather. */
 DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
 /* Device workspace bytes of disco_fused_conv: the bf16 intermediate
    X[B, Cin, K, H_out, W_out] when the tensor-core contraction takes the shape
-   (bf16, W_in % 8 == 0, s in {1, 2}, K <= 9), else 0 (no workspace needed). */
+   (bf16, W_in % 8 == 0, W_in >= 64, s in {1, 2}, K <= 9), else 0 (no
+   workspace needed). */
 DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
                                                   disco_dtype dtype);
 

@@ -49,7 +49,8 @@ constexpr int kBuilderThreads = 192;   // warps 2..7
 constexpr int kTW = 16;                // output columns per MMA tile
 constexpr int kCK = 4;                 // K steps (16 window columns) per chunk
 constexpr int kChunkCols = kCK * 16;   // 64
-constexpr uint32_t kGroupBytes = 128 * 16;  // one TMA box: 128 rows x 8 bf16
+constexpr uint32_t kBoxBytes = 128 * 128;   // one wide TMA box: 128 rows x 64 bf16 (128-byte swizzle)
+constexpr uint32_t kNarrowBytes = 128 * 16; // one narrow box: 128 rows x 8 bf16 (no swizzle)
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusTcTimeout = 4;
 
@@ -128,15 +129,15 @@ __device__ __forceinline__ RunGeom run_geom(const disco_run& r, int Win) {
 template <int K, int S, int STAGES>
 struct TcCfg {
   static constexpr int N = 16 * K;                           // MMA N
-  static constexpr uint32_t kBBytes = N * kChunkCols * 2;    // B chunk
-  static constexpr uint32_t kSBOB = (kChunkCols / 8) * 128;  // 1024
+  static constexpr uint32_t kBBytes = N * kChunkCols * 2;    // B chunk (128-byte rows)
   static constexpr int NT = (512 / N) < 4 ? (512 / N) : 4;   // tiles per CTA
-  static constexpr int AG = (kChunkCols + S * kTW * (NT - 1)) / 8;  // A groups per stage
-  static constexpr uint32_t kABytes = AG * kGroupBytes;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  // 64-column boxes covering the chunk's window for all NT tiles
+  static constexpr int NBOX = (kChunkCols + S * kTW * (NT - 1) + 63) / 64;
+  static constexpr uint32_t kABytes = NBOX * kBoxBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // multiple of 1024
   static constexpr uint32_t kTmemCols = (NT * N <= 32) ? 32 : (NT * N <= 64) ? 64 : (NT * N <= 128) ? 128
                                         : (NT * N <= 256) ? 256 : 512;
-  static constexpr size_t kFixed = (size_t)STAGES * kStageBytes + 256;
+  static constexpr size_t kFixed = (size_t)STAGES * kStageBytes + 256 + 1024;  // + alignment slack
   // two psi table buffers (double-buffered across runs): K rows x TLB bf16 each
   __host__ __device__ static size_t tab_bytes(int TLB) { return ((size_t)K * TLB * 2 + 127) & ~(size_t)127; }
   static size_t smem(int TLB) { return kFixed + 2 * tab_bytes(TLB); }
@@ -144,10 +145,13 @@ struct TcCfg {
 
 template <int K, int S, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xnarrow,
+                  const TcArgs a) {
   using Cfg = TcCfg<K, S, STAGES>;
   constexpr int N = Cfg::N, NT = Cfg::NT;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::kStageBytes);
   uint64_t* fullA = bars;                 // [STAGES] TMA bytes landed
   uint64_t* fullB = bars + STAGES;        // [STAGES] B chunk built (192 arrivals)
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 6);
   // psi tables of two consecutive runs: [2][K][TLB] bf16
-  uint8_t* tabs = smem + Cfg::kFixed;
+  uint8_t* tabs = smem + STAGES * Cfg::kStageBytes + 256;
   const size_t tab_bytes = Cfg::tab_bytes(a.TLB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -224,12 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int nks = min(kCK, g.KS - c * kCK);
-          const int ng = (S * kTW * (NT - 1) + 16 * nks) / 8;
+          // boxes holding window columns [64 c, 64 c + 16 nks + S*16*(NT-1))
+          const int nbox = (16 * nks + S * kTW * (NT - 1) + 63) / 64;
           uint8_t* sA = smem + s * Cfg::kStageBytes;
-          mbar_expect_tx(&fullA[s], ng * kGroupBytes);
-          for (int gi = 0; gi < ng; ++gi) {
-            const int col = wrap_col(u0 + c * kChunkCols + 8 * gi, a.Win);
-            tma_load_3d(sA + gi * kGroupBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+          mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
+          for (int bb = 0; bb < nbox; ++bb) {
+            const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
+            if (col + 64 <= a.Win) {
+              tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+            } else {  // crosses the longitude seam: 8 wrapped narrow boxes
+              for (int gi = 0; gi < 8; ++gi)
+                tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow,
+                            wrap_col(col + 8 * gi, a.Win), g.hi, bc0, &fullA[s]);
+            }
           }
         }
       }
@@ -263,12 +274,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nks = min(kCK, g.KS - c * kCK);
           const uint32_t abase = smem_u32(smem + s * Cfg::kStageBytes);
           const uint32_t bbase = abase + Cfg::kABytes;
+          const int u0 = S * wc - g.M;
+          bool narrow[Cfg::NBOX];
+#pragma unroll
+          for (int bb = 0; bb < Cfg::NBOX; ++bb)
+            narrow[bb] = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win) + 64 > a.Win;
           for (int j = 0; j < NT; ++j)
             for (int ks = 0; ks < nks; ++ks) {
-              // A: LBO (next 8 columns) = one 2 KB group, SBO (next 8 rows) = 128 B
-              const uint64_t ad = smem_desc(abase + (uint32_t)(2 * S * j + 2 * ks) * kGroupBytes,
-                                            kGroupBytes, 128);
-              const uint64_t bd = smem_desc(bbase + ks * 256, 128, Cfg::kSBOB);
+              // window column of the K step inside the stage, its box and its step in the box
+              const int col = 16 * ks + S * kTW * j;
+              const int bb = col >> 6, ka = (col & 63) >> 4;
+              bool nb = false;
+#pragma unroll
+              for (int q = 0; q < Cfg::NBOX; ++q)
+                if (q == bb) nb = narrow[q];
+              const uint32_t slot = abase + bb * kBoxBytes;
+              const uint64_t ad = nb ? smem_desc(slot + ka * 2 * kNarrowBytes, kNarrowBytes, 128)
+                                     : smem_desc_sw128(slot + 32 * ka);
+              const uint64_t bd = smem_desc_sw128(bbase + 32 * ks);
               umma_bf16(tmem + j * N, ad, bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
             }
           umma_commit(&empty[s]);
@@ -325,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) w[e] = (uint32_t)v[2 * e] | ((uint32_t)v[2 * e + 1] << 16);
           }
-          *reinterpret_cast<uint4*>(sB + (n >> 3) * Cfg::kSBOB + gi * 128 + (n & 7) * 16) =
+          *reinterpret_cast<uint4*>(sB + n * 128 + ((gi ^ (n & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
@@ -366,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<uint4*>(dst)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
                 reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
               } else {
-                for (int e = 0; e < n; ++e) dst[e] = __float2bfloat16_rn(v[e]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (e < n) dst[e] = __float2bfloat16_rn(v[e]);
               }
             }
           }
@@ -396,7 +421,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int K, int S, int STAGES>
-int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, TcArgs a, cudaStream_t st) {
+int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, const CUtensorMap& nmap, TcArgs a,
+                     cudaStream_t st) {
   using Cfg = TcCfg<K, S, STAGES>;
   const size_t smem = Cfg::smem(a.TLB);
   auto kern = fwd_tc_kernel<K, S, STAGES>;
@@ -404,7 +430,7 @@ int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, TcArgs a, cud
       cudaSuccess)
     return check_launch("disco_fwd (tensor cores) attribute");
   dim3 grid((a.Wout + kTW * Cfg::NT - 1) / (kTW * Cfg::NT), (a.BC + 127) / 128, a.Hout);
-  kern<<<grid, kThreads, smem, st>>>(map, a);
+  kern<<<grid, kThreads, smem, st>>>(map, nmap, a);
   return check_launch("disco_fwd (tensor cores)");
 }
 
@@ -430,16 +456,20 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
   if (!fit2) return DISCO_ERR_UNSUPPORTED;
   auto enc = encode_fn();
   if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  CUtensorMap map;
+  CUtensorMap map, nmap;
   cuuint64_t dims[3] = {(cuuint64_t)Win, (cuuint64_t)Hin, (cuuint64_t)BC};
   cuuint64_t strides[2] = {(cuuint64_t)Win * 2, (cuuint64_t)Hin * Win * 2};
-  cuuint32_t box[3] = {8, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
-  return fit3 ? launch_tc_stages<K, S, 3>(psi, map, a, st) : launch_tc_stages<K, S, 2>(psi, map, a, st);
+  for (int m = 0; m < 2; ++m) {
+    cuuint32_t box[3] = {m == 0 ? 64u : 8u, 1, 128};
+    CUresult cr = enc(m == 0 ? &map : &nmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims,
+                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      m == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  }
+  return fit3 ? launch_tc_stages<K, S, 3>(psi, map, nmap, a, st)
+              : launch_tc_stages<K, S, 2>(psi, map, nmap, a, st);
 }
 
 template <int K, int S>
@@ -465,7 +495,8 @@ cudaError_t tc_status(int32_t* v, bool clear) {
 
 // True when fwd_tensor_core takes this psi and channel count.
 bool fwd_tc_supported(const disco_psi* psi, int BC) {
-  if (psi->grid_in.nlon % 8 != 0 || (psi->s != 1 && psi->s != 2) || BC < 1 || BC > 65535 * 128 ||
+  if (psi->grid_in.nlon % 8 != 0 || psi->grid_in.nlon < 64 || (psi->s != 1 && psi->s != 2) || BC < 1 ||
+      BC > 65535 * 128 ||
       !psi->ftab || !psi->ftab_off || psi->K < 1 || psi->K > 9)
     return false;
 #define DISCO_TFIT(KK) \

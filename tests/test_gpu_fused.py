@@ -147,11 +147,11 @@ def test_fused_workload_sampled_full_size(lib, name):
 
 
 def test_fused_rejects_unsupported(lib):
-    gi, go = (16, 32, 0), (16, 32, 0)
+    gi, go = (16, 64, 0), (16, 64, 0)  # tensor-core path (W_in % 8 == 0, W_in >= 64)
     psi = lib.Psi(gi, go, 0, 3, 2 * math.pi / 16)
-    x = torch.zeros((1, 8, 16, 32), dtype=BF, device="cuda")
+    x = torch.zeros((1, 8, 16, 64), dtype=BF, device="cuda")
     W = torch.zeros((8, 8, 3), dtype=BF, device="cuda")
-    y = torch.zeros((1, 8, 16, 32), dtype=BF, device="cuda")
+    y = torch.zeros((1, 8, 16, 64), dtype=BF, device="cuda")
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_fused_conv(psi.c, x, W, y, 1, 8, 8)  # no workspace for the tensor-core path
     assert e.value.status == -7
