@@ -252,15 +252,17 @@ def run_ours(args):
     value = ws * (alg["fwd_bytes"] + alg["bwd_bytes"]) * args.steps / (contr_ms * 1e6)
     med = {k: statistics.median(v) for k, v in per.items()}
     share = {k: sum(v) for k, v in per.items()}
-    dom = max(share, key=share.get)
     clocks = clk.summary()
-    # dominant kernel: plain FP32 FMA arithmetic (CUDA cores); peak = SMs x
-    # 128 FP32 lanes x 2 flops x the measured median SM clock under load
-    sm_mhz = clocks["sm_mhz"] or peaks.get("sm_max_mhz", 2070.0)
-    alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-    dom_flops = alg["csr_flops"]  # fwd, bwd and the fused gather share the CSR FMA count
-    achieved = dom_flops / (med[dom] * 1e-3) / 1e12
-    traffic = _traffic_from_profiles(dom)
+    # Dominant kernel: the transpose (bwd_tc_kernel) or forward (fwd_tc_kernel)
+    # contraction, each launched twice per step (disco_bwd / disco_fwd alone
+    # and inside the fused calls); the disco_bwd and disco_fwd calls are one
+    # launch each, so their events time the kernel alone.  Bound: HBM, with
+    # the algorithmic bytes of one launch (input + output + psi).
+    dom = "bwd" if med["bwd"] >= med["fwd"] else "fwd"
+    dom_kernel = {"bwd": "bwd_tc_kernel", "fwd": "fwd_tc_kernel"}[dom]
+    dom_bytes = alg[dom + "_bytes"]
+    achieved = dom_bytes / (med[dom] * 1e-3) / 1e9
+    traffic = _traffic_from_profiles(dom_kernel, w.name)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
@@ -275,10 +277,12 @@ def run_ours(args):
         "fused_conv_ms_per_call": round(med["fused"], 3),
         "fused_conv_bwd_input_ms_per_call": round(med["fused_bwd"], 3),
         "kernel_ms": {k: round(v, 3) for k, v in med.items()},
-        "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2),
-                     "peak": round(alu_peak, 2), "unit": "TFLOP/s",
-                     "frac": round(achieved / alu_peak, 4), "traffic": traffic,
-                     "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz (measured clock)"},
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "ms_per_launch": round(med[dom], 3),
+                     "peak_source": f"{peak_src} (copy bandwidth)"},
         "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peak_src,
         "clocks": clocks, "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
     }
@@ -289,14 +293,22 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _traffic_from_profiles(kernel: str):
-    """DRAM bytes per launch of `kernel`, taken from a committed ncu summary
-    (profiles/traffic.json) when it matches the current sources, else None."""
+def _traffic_from_profiles(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    record profiles/traffic.json, or None when there is none for this
+    workload or the kernel's source changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        return t.get(kernel)
+        if t.get("workload") != workload:
+            return None
+        e = t["kernels"][kernel]
+        with open(os.path.join(ROOT, e["source"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != e["sha1"]:
+                return None
+        return int(e["dram_read"]) + int(e["dram_write"])
     except Exception:
         return None
 
