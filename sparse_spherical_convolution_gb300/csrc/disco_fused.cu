@@ -617,6 +617,9 @@ static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y,
                     int32_t Cout, void* X, cudaStream_t s) {
   int st = fwd_tensor_core(psi, x, X, B * Cin, s);
   if (st) return st;
+  const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
+  st = einsum_tensor_core(X, W, y, B, Cin * psi->K, Cout, P, s);
+  if (st != DISCO_ERR_UNSUPPORTED) return st;
   EinArgs e;
   e.X = (const __nv_bfloat16*)X;
   e.W = (const __nv_bfloat16*)W;
@@ -702,13 +705,17 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   g.CK = Cin * psi->K;
   g.P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaFuncSetAttribute(dx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kGSmem) != cudaSuccess)
-    return check_launch("dX gemm attribute");
-  dim3 grid((g.CK + kGN - 1) / kGN, (unsigned)((g.P + kGM - 1) / kGM), B);
-  if (grid.y > 65535) return fail(DISCO_ERR_UNSUPPORTED, "H_out * W_out too large");
-  dx_gemm_kernel<<<grid, kGThreads, kGSmem, s>>>(g);
-  if ((st = check_launch("dX gemm"))) return st;
+  st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s);
+  if (st == DISCO_ERR_UNSUPPORTED) {
+    if (cudaFuncSetAttribute(dx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGSmem) != cudaSuccess)
+      return check_launch("dX gemm attribute");
+    dim3 grid((g.CK + kGN - 1) / kGN, (unsigned)((g.P + kGM - 1) / kGM), B);
+    if (grid.y > 65535) return fail(DISCO_ERR_UNSUPPORTED, "H_out * W_out too large");
+    dx_gemm_kernel<<<grid, kGThreads, kGSmem, s>>>(g);
+    st = check_launch("dX gemm");
+  }
+  if (st) return st;
   return disco_bwd(psi, workspace, gx, B, Cin, dtype, stream);
 }
 
@@ -724,6 +731,7 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
   }
   if (e == cudaSuccess) e = tc_status(flags, clear != 0);
   if (e == cudaSuccess) e = btc_status(flags, clear != 0);
+  if (e == cudaSuccess) e = gemm_status(flags, clear != 0);
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
   return DISCO_OK;
 }

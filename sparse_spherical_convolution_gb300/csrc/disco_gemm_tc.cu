@@ -1,0 +1,379 @@
+// disco_gemm_tc.cu -- the dense contractions of the fused paths on the tensor
+// cores: the channel/basis einsum of the fused convolution and the dX GEMM of
+// its input gradient.
+//
+// DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
+// ("_disco_s2_fused_conv_optimized: contraction + einsum"): after the S2
+// contraction, y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo].  Both GEMMs
+// here have the form
+//
+//   out[b, n, p] = sum_j A[b, j, p] * Bop(j, n)        (p = pixel ho*W_out + wo)
+//
+//   einsum: A = X  [B][C*K][P],   Bop(j, n) = W[n][j]   (n = o,  j = c*K + k)
+//   dX:     A = dy [B][Cout][P],  Bop(j, n) = W[j][n]   (n = c*K + k, j = o)
+//
+// as one tcgen05 GEMM per tile of 128 pixels x N (<= 256) outputs: M = 128
+// pixels, accumulators in TMEM.  A is read by TMA straight from its natural
+// layout as "MN-major" tiles (pixels contiguous; two 64-pixel boxes of 64
+// j-rows per stage, 128-byte swizzle); Bop is K-major (einsum: W rows) or
+// MN-major (dX: W rows are j), also by TMA.  Persistent kernel, 4-stage
+// load ring, two TMEM accumulators so the epilogue of one tile overlaps the
+// main loop of the next:
+//   warp 0  TMA producer (one thread),
+//   warp 1  MMA issuer (one thread, TMEM owner),
+//   warps 2-5 epilogue: tcgen05.ld, bf16, stores coalesced along pixels.
+// All mbarrier waits are bounded (time-out -> status flag, abort).
+
+#include <cudaTypedefs.h>
+
+#include "disco_internal.cuh"
+#include "disco_umma.cuh"
+
+namespace disco {
+
+__device__ int g_gemm_status = 0;
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kBM = 128;                  // pixels per tile
+constexpr int kBK = 64;                   // j per stage
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB: two 64-pixel boxes
+constexpr uint32_t kBMax = 256 * kBK * 2;     // 32 KB: up to 256 outputs
+constexpr uint32_t kStageBytes = kABytes + kBMax;
+constexpr uint32_t kEpiStage = 16 * 32 * 2;      // per epilogue warp: 16 outputs x 32 pixels bf16
+constexpr size_t kSmem = (size_t)kStages * kStageBytes + 4 * kEpiStage + 256 + 1024;
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kStatusGemmTimeout = 2;
+
+__device__ __forceinline__ void gemm_flag() { atomicOr(&g_gemm_status, kStatusGemmTimeout); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 128-byte swizzled operand tile descriptor with explicit LBO / SBO (bytes)
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// kind::f16 instruction descriptor, bf16 A and B, fp32 D; A MN-major, B as given
+__host__ __device__ constexpr uint32_t idesc_mn(int M, int N, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct GemmTcArgs {
+  __nv_bfloat16* out;  // [B][Nt][P]
+  int64_t P;           // pixels
+  int Kt;              // reduction length j
+  int Nt;              // outputs n
+  int NB;              // outputs per tile (multiple of 16, <= 256)
+  int mt, nt, B;       // tiles along pixels, along n, batch
+};
+
+template <bool kBMN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                   const GemmTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint16_t* epi_stage = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kEpiStage);
+  uint64_t* full = bars;                   // [kStages]
+  uint64_t* empty = bars + kStages;        // [kStages]
+  uint64_t* accf = bars + 2 * kStages;     // [2] accumulator complete (commit)
+  uint64_t* acce = bars + 2 * kStages + 2; // [2] accumulator drained (128 arrivals)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = a.mt * a.nt * a.B;
+  const int nk = (a.Kt + kBK - 1) / kBK;
+  const uint32_t bbytes = (uint32_t)a.NB * kBK * 2;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiThreads);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // tile t: n tiles fastest (consecutive CTAs share the A tile in L2), then pixels, then batch
+  auto coords = [&](int t, int* p0, int* n0, int* b) {
+    *n0 = (t % a.nt) * a.NB;
+    const int r = t / a.nt;
+    *p0 = (r % a.mt) * kBM;
+    *b = r / a.mt;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      int i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int p0, n0, b;
+        coords(t, &p0, &n0, &b);
+        for (int kc = 0; kc < nk; ++kc, ++i) {
+          const int s = i % kStages;
+          if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          mbar_expect_tx(&full[s], kABytes + bbytes);
+          tma_load_3d(sa, &amap, p0, kc * kBK, b, &full[s]);
+          tma_load_3d(sa + kABytes / 2, &amap, p0 + 64, kc * kBK, b, &full[s]);
+          if (kBMN) {
+            for (int q = 0; q < a.NB / 64; ++q)  // W rows j, 64 outputs per box
+              tma_load_2d(sb + q * (64 * kBK * 2), &bmap, n0 + 64 * q, kc * kBK, &full[s]);
+          } else {
+            tma_load_2d(sb, &bmap, kc * kBK, n0, &full[s]);  // NB W rows of 64 j
+          }
+        }
+      }
+      if (!ok) {
+        gemm_flag();
+        *abort_flag = 1;
+        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
+          const int li = i - back;
+          mbar_wait(&full[li % kStages], (li / kStages) & 1, kWaitLimit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      const uint32_t idesc = idesc_mn(kBM, a.NB, kBMN);
+      int i = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+        const int ab = tl & 1;  // accumulator buffer
+        if (tl >= 2 && !mbar_wait(&acce[ab], ((tl >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + ab * 256;
+        for (int kc = 0; kc < nk; ++kc, ++i) {
+          const int s = i % kStages;
+          if (!mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            // A: 16 j-rows = two 8-row groups (SBO 1024) further; second pixel half at LBO 8 KB
+            const uint64_t ad = desc_sw128(sa + ks * 2048, kABytes / 2, 1024);
+            const uint64_t bd = kBMN ? desc_sw128(sb + ks * 2048, 64 * kBK * 2, 1024)
+                                     : desc_sw128(sb + ks * 32, 16, 1024);
+            umma_bf16(d, ad, bd, idesc, (kc > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&accf[ab]);
+      }
+      if (!ok) {
+        gemm_flag();
+        *abort_flag = 1;
+        if (i > 0) mbar_wait(&empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, kWaitLimit);
+      }
+    }
+  } else {
+    // ------------------------------------------------- epilogue (warps 2-5) --
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+    int tl = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+      const int ab = tl & 1;
+      bool fin = mbar_wait(&accf[ab], (tl >> 1) & 1, kWaitLimit);
+      fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
+      if (!fin) {
+        if (lane == 0) gemm_flag();
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      int p0, n0, b;
+      coords(t, &p0, &n0, &b);
+      // 16 outputs x 32 pixels at a time through shared memory, so that each
+      // lane then stores 16 consecutive bytes (8 pixels) of one output row
+      const int64_t pw = p0 + q * 32;  // this warp's first pixel
+      uint16_t* stg = epi_stage + (warp - 2) * (kEpiStage / 2);
+      __nv_bfloat16* ob = a.out + (size_t)b * a.Nt * a.P;
+      for (int c0 = 0; c0 < a.NB; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + ab * 256 + ((uint32_t)(q * 32) << 16) + c0, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v[e]));
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int idx = lane + 32 * h, row = idx >> 2, seg = idx & 3;
+          const int n = n0 + c0 + row;
+          const int64_t pp = pw + seg * 8;  // P % 8 == 0: a segment is all in or all out
+          if (n < a.Nt && pp < a.P)
+            *reinterpret_cast<uint4*>(ob + (size_t)n * a.P + pp) =
+                *reinterpret_cast<const uint4*>(stg + row * 32 + seg * 8);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(&acce[ab]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+           const cuuint32_t* box) {
+  auto enc = encode_fn_g();
+  if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  return DISCO_OK;
+}
+
+int sm_count_g() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 1;
+  }
+  return n;
+}
+
+// out[b][n][p] = sum_j A[b][j][p] * Bop(j, n); W is [Nt][Kt] (kBMN false) or [Kt][Nt] (true)
+template <bool kBMN>
+int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, int64_t P, cudaStream_t st) {
+  GemmTcArgs g;
+  g.out = (__nv_bfloat16*)out;
+  g.P = P;
+  g.Kt = Kt;
+  g.Nt = Nt;
+  g.NB = kBMN ? (Nt >= 256 ? 256 : (Nt + 63) / 64 * 64) : (Nt + 15) / 16 * 16;
+  g.mt = (int)((P + kBM - 1) / kBM);
+  g.nt = (Nt + g.NB - 1) / g.NB;
+  g.B = B;
+  CUtensorMap amap, bmap;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)Kt, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)Kt * P * 2};
+    cuuint32_t box[3] = {64, kBK, 1};
+    int s = encode(&amap, A, 3, dims, strides, box);
+    if (s) return s;
+  }
+  {
+    cuuint64_t dims[2] = {kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt, kBMN ? (cuuint64_t)Kt : (cuuint64_t)Nt};
+    cuuint64_t strides[1] = {(kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt) * 2};
+    cuuint32_t box[2] = {64, kBMN ? (cuuint32_t)kBK : (cuuint32_t)g.NB};
+    int s = encode(&bmap, W, 2, dims, strides, box);
+    if (s) return s;
+  }
+  auto kern = gemm_tc_kernel<kBMN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
+    return check_launch("tensor-core GEMM attribute");
+  const long long ntiles = (long long)g.mt * g.nt * B;
+  if (ntiles > 0x7fffffffLL) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
+  const int grid = (int)(ntiles < sm_count_g() ? ntiles : sm_count_g());
+  kern<<<grid, kThreads, kSmem, st>>>(amap, bmap, g);
+  return check_launch("tensor-core GEMM");
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int64_t P, int Kt, int Nt) {
+  return P % 8 == 0 && P >= 128 && Kt % 8 == 0 && Kt >= kBK && Nt % 8 == 0 && Nt >= 16;
+}
+
+int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P, cudaStream_t st) {
+  if (!gemm_tc_supported(P, CK, Cout) || Cout > 256) return DISCO_ERR_UNSUPPORTED;
+  return launch_gemm<false>(X, W, y, B, CK, Cout, P, st);
+}
+
+int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P, cudaStream_t st) {
+  if (!gemm_tc_supported(P, Cout, CK) || CK % 64 != 0) return DISCO_ERR_UNSUPPORTED;
+  return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st);
+}
+
+cudaError_t gemm_status(int32_t* v, bool clear) {
+  int32_t t = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&t, g_gemm_status, sizeof(int32_t));
+  if (e == cudaSuccess && clear) {
+    const int32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(int32_t));
+  }
+  *v |= t;
+  return e;
+}
+
+}  // namespace disco

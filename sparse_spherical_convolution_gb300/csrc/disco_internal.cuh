@@ -37,6 +37,16 @@ cudaError_t tc_status(int32_t* v, bool clear);
 int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st);
 cudaError_t btc_status(int32_t* v, bool clear);
 
+// Dense GEMMs of the fused paths on the tensor cores (TMA-fed tcgen05):
+//   einsum: y[b][o][p] = sum_j X[b][j][p] W[o][j]   (j = c*K + k)
+//   dX:     dX[b][j][p] = sum_o dy[b][o][p] W[o][j]
+// DISCO_ERR_UNSUPPORTED, without launching, for shapes they do not take.
+int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P,
+                       cudaStream_t st);
+int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P,
+                   cudaStream_t st);
+cudaError_t gemm_status(int32_t* v, bool clear);
+
 // Geometry of the transpose tables by input-row group (disco_psi.grp_ptr):
 // 8 input rows per group, 64-column chunks, TQ = 32 / s decimated output
 // columns per tile block, table rows of CW = roundup8(63 + TQ) elements.
