@@ -34,6 +34,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "disco_internal.cuh"
 #include "disco_umma.cuh"
 
@@ -97,6 +99,7 @@ struct TcArgs {
   const uint16_t* ftab;  // per run: K rows of TL = roundup8(len + 16), psi_k(delta) at 8 + delta - dlo
   int BC, Hout, Wout, Win;
   int TLB;            // table row capacity (>= every run's row length)
+  int tma_store;      // X written by TMA stores (W_out % 8 == 0 and W_out >= one tile's columns)
 };
 
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -138,6 +141,11 @@ struct TcCfg {
   static constexpr uint32_t kTmemCols = (NT * N <= 32) ? 32 : (NT * N <= 64) ? 64 : (NT * N <= 128) ? 128
                                         : (NT * N <= 256) ? 256 : 512;
   static constexpr size_t kFixed = (size_t)STAGES * kStageBytes + 256 + 1024;  // + alignment slack
+  // the epilogue stages the X tile [K][128 channels][NT*16 columns] (bf16) in
+  // the freed pipeline buffers and writes it with TMA stores when it fits
+  static constexpr uint32_t kOutRow = NT * kTW * 2;            // bytes of one channel row
+  static constexpr uint32_t kOutBytes = (uint32_t)K * 128 * kOutRow;
+  static constexpr bool kTmaStore = kOutBytes <= (uint32_t)STAGES * kStageBytes;
   // two psi table buffers (double-buffered across runs): K rows x TLB bf16 each
   __host__ __device__ static size_t tab_bytes(int TLB) { return ((size_t)K * TLB * 2 + 127) & ~(size_t)127; }
   static size_t smem(int TLB) { return kFixed + 2 * tab_bytes(TLB); }
@@ -146,7 +154,7 @@ struct TcCfg {
 template <int K, int S, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xnarrow,
-                  const TcArgs a) {
+                  const __grid_constant__ CUtensorMap outmap, const TcArgs a) {
   using Cfg = TcCfg<K, S, STAGES>;
   constexpr int N = Cfg::N, NT = Cfg::NT;
   extern __shared__ uint8_t smem_raw[];
@@ -363,6 +371,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
       if (!fin) {
         if (lane == 0) tc_flag(kStatusTcTimeout);
+      } else if (Cfg::kTmaStore && a.tma_store) {
+        tc_fence_after();
+        // X tile through shared memory (the pipeline buffers are free once every
+        // MMA has completed), then one TMA store per k of [128 channels x NT*16
+        // columns]; the store clips columns >= W_out and channels >= B*C
+        const int r = q * 32 + lane;
+        for (int k = 0; k < K; ++k)
+          for (int j = 0; j < NT; ++j) {
+            float v[16];
+            if (items > 0) {
+              tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + j * N + k * 16, v);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] = 0.f;
+            }
+            uint32_t w32[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+              w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(smem + ((size_t)k * 128 + r) * Cfg::kOutRow + j * kTW * 2);
+            dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
+            dst[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
+          }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (warp == 4 && lane == 0) {
+          for (int k = 0; k < K; ++k)
+            asm volatile(
+                "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                    reinterpret_cast<uint64_t>(&outmap)),
+                "r"(wc), "r"(k * a.Hout + ho), "r"(bc0), "r"(smem_u32(smem + (size_t)k * 128 * Cfg::kOutRow))
+                : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // shared memory read out
+        }
       } else {
         tc_fence_after();
         const int bc = bc0 + q * 32 + lane;
@@ -421,8 +466,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int K, int S, int STAGES>
-int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, const CUtensorMap& nmap, TcArgs a,
-                     cudaStream_t st) {
+int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, const CUtensorMap& nmap,
+                     const CUtensorMap& omap, TcArgs a, cudaStream_t st) {
   using Cfg = TcCfg<K, S, STAGES>;
   const size_t smem = Cfg::smem(a.TLB);
   auto kern = fwd_tc_kernel<K, S, STAGES>;
@@ -430,7 +475,7 @@ int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, const CUtenso
       cudaSuccess)
     return check_launch("disco_fwd (tensor cores) attribute");
   dim3 grid((a.Wout + kTW * Cfg::NT - 1) / (kTW * Cfg::NT), (a.BC + 127) / 128, a.Hout);
-  kern<<<grid, kThreads, smem, st>>>(map, nmap, a);
+  kern<<<grid, kThreads, smem, st>>>(map, nmap, omap, a);
   return check_launch("disco_fwd (tensor cores)");
 }
 
@@ -468,8 +513,21 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
   }
-  return fit3 ? launch_tc_stages<K, S, 3>(psi, map, nmap, a, st)
-              : launch_tc_stages<K, S, 2>(psi, map, nmap, a, st);
+  // X as the TMA store target: [B*C][K*H_out][W_out], box NT*16 columns x 1 row x 128 channels
+  CUtensorMap omap;
+  constexpr int NT3 = TcCfg<K, S, 3>::NT;
+  a.tma_store = (a.Wout % 8 == 0 && a.Wout >= NT3 * kTW) ? 1 : 0;
+  memset(&omap, 0, sizeof(omap));
+  if (a.tma_store) {
+    cuuint64_t od[3] = {(cuuint64_t)a.Wout, (cuuint64_t)K * a.Hout, (cuuint64_t)BC};
+    cuuint64_t os[2] = {(cuuint64_t)a.Wout * 2, (cuuint64_t)K * a.Hout * a.Wout * 2};
+    cuuint32_t ob[3] = {(cuuint32_t)(NT3 * kTW), 1, 128};
+    CUresult cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, X, od, os, ob, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  }
+  return fit3 ? launch_tc_stages<K, S, 3>(psi, map, nmap, omap, a, st)
+              : launch_tc_stages<K, S, 2>(psi, map, nmap, omap, a, st);
 }
 
 template <int K, int S>
