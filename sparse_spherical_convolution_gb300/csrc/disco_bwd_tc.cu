@@ -121,7 +121,8 @@ struct BCfg {
   // stage: 2 G box slots | T chunk | psi block
   static constexpr uint32_t kStageBytes = 2 * kBoxBytes + kTBytes + kTabSlot;
   static constexpr uint32_t kInfoBytes = 2 * kMaxEnt * sizeof(disco_grp_ent);
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + kInfoBytes + 256 + 1024;
+  static constexpr uint32_t kOutBytes = 128 * 32 * 2;  // one gx piece: 128 channels x 32 columns
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kOutBytes + kInfoBytes + 256 + 1024;
 };
 
 // the z-th row group in processing order: poles first, then inwards
@@ -144,7 +145,7 @@ __device__ __forceinline__ bool box_is_narrow(int col0, int Wout) { return wrapc
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap gwide, const __grid_constant__ CUtensorMap gnarrow,
-                  const BtcArgs a) {
+                  const __grid_constant__ CUtensorMap gxmap, const BtcArgs a) {
   using Cfg = BCfg<S>;
   constexpr int TQ = Cfg::TQ, CW = Cfg::CW;
   constexpr int kStep1 = TQ / 16;  // K steps between the two blocks' windows
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   disco_grp_ent* infos = reinterpret_cast<disco_grp_ent*>(smem + kStages * Cfg::kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * Cfg::kStageBytes + Cfg::kInfoBytes);
+  uint8_t* outbuf = smem + kStages * Cfg::kStageBytes + Cfg::kInfoBytes;  // [2] gx pieces for TMA stores
+  uint64_t* bars = reinterpret_cast<uint64_t*>(outbuf + 2 * Cfg::kOutBytes);
   uint64_t* fullA = bars;                         // [kStages] G boxes + psi block landed
   uint64_t* fullB = bars + kStages;               // [kStages] T built (192 arrivals)
   uint64_t* empty = bars + 2 * kStages;           // [kStages] MMAs of the stage done (commit)
@@ -375,11 +377,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------- epilogue (warps 8-11) --
     const int q = warp & 3;
-    int tl = 0;
+    int tl = 0, npiece = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
       const int b = tl & 1;
-      bool fin = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) && mbar_wait(acc_full, tl & 1, kWaitLimit);
-      fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
+      bool fin = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) &&
+                 mbar_wait(acc_full, tl & 1, kWaitLimit) && !*abort_flag;
+      // one decision for all 4 epilogue warps: they meet at named barriers below
+      fin = all_named(fin, 2, kEpiThreads);
       if (!fin) {
         if (lane == 0) btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
@@ -390,10 +394,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords<S>(a, tile, &qb, &bc0, &zg);
       const int hi0 = zg * kGrpRows;
       const bool any = info_cnt[b] > 0;
-      const int bc = bc0 + q * 32 + lane;
+      const int er = q * 32 + lane;  // channel row of this thread in a piece
+      // 16 pieces of [128 channels x 32 columns] (one row, one column block),
+      // each converted into one of two shared-memory buffers and written by a
+      // TMA store (rows >= H_in and channels >= B*C are clipped by the store)
       for (int blk = 0; blk < kNT; ++blk)
-        for (int r = 0; r < kGrpRows; ++r) {
-          const int hi = hi0 + r;
+        for (int r = 0; r < kGrpRows; ++r, ++npiece) {
+          uint8_t* ob = outbuf + (npiece & 1) * Cfg::kOutBytes;
+          if (tid == 256) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // buffer free
+          asm volatile("bar.sync 2, 128;" ::: "memory");
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             float v[16];
@@ -403,25 +412,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) v[e] = 0.f;
             }
-            const int col = S * (qb + blk * TQ) + cc * 16;
-            if (hi < a.Hin && bc < a.BC && col < a.Win) {
-              __nv_bfloat16* dst = a.gx + ((size_t)bc * a.Hin + hi) * a.Win + col;
-              uint32_t w32[8];
+            uint32_t w32[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                w32[e] = *reinterpret_cast<uint32_t*>(&p2);
-              }
-              reinterpret_cast<uint4*>(dst)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
-              if (col + 16 <= a.Win)  // W_in is a multiple of 8
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
+            for (int e = 0; e < 8; ++e) {
+              __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+              w32[e] = *reinterpret_cast<uint32_t*>(&p2);
             }
+            uint4* dst = reinterpret_cast<uint4*>(ob + er * 64 + cc * 32);
+            dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
+            dst[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
+          }
+          fence_proxy_async_smem();
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+          if (tid == 256) {
+            const int col = S * (qb + blk * TQ);
+            if (col < a.Win && hi0 + r < a.Hin)  // else the whole piece lies outside gx
+              asm volatile(
+                  "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                      reinterpret_cast<uint64_t>(&gxmap)),
+                  "r"(col), "r"(hi0 + r), "r"(bc0), "r"(smem_u32(ob))
+                  : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
       tc_fence_before();
       mbar_arrive(tmem_empty);
       mbar_arrive(&info_empty[b]);
     }
+    if (tid == 256) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -489,16 +507,27 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
   a.ntx = (a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ);
   a.nty = (BC + 127) / 128;
   a.ntz = psi->ngrp;
-  CUtensorMap wide, narrow;
+  CUtensorMap wide, narrow, gxm;
   int stt = encode_g(&wide, G, a, BC, 64, true);
   if (stt) return stt;
   if ((stt = encode_g(&narrow, G, a, BC, 8, false))) return stt;
+  {
+    // gx as the TMA store target: [B*C][H_in][W_in], box 32 columns x 1 row x 128 channels
+    cuuint64_t dims[3] = {(cuuint64_t)a.Win, (cuuint64_t)a.Hin, (cuuint64_t)BC};
+    cuuint64_t strides[2] = {(cuuint64_t)a.Win * 2, (cuuint64_t)a.Hin * a.Win * 2};
+    cuuint32_t box[3] = {32, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult cr = encode_fn_b()(&gxm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, gx, dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  }
   auto kern = bwd_tc_kernel<S>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) != cudaSuccess)
     return check_launch("disco_bwd (tensor cores) attribute");
   const long long ntiles = (long long)a.ntx * a.nty * a.ntz;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
-  kern<<<grid, kThreads, Cfg::kSmem, st>>>(wide, narrow, a);
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(wide, narrow, gxm, a);
   return check_launch("disco_bwd (tensor cores)");
 }
 
