@@ -8,7 +8,8 @@ shares no code with the CUDA path.  The arithmetic lives in ``disco_oracle.c``
 Pinned by the ``not gpu`` tests (dense brute force with independent vector
 geometry, adjoint identity, longitude equivariance, the indicator-basis
 neighbourhood sum, normalisation and symmetry invariants, hand-derived closed
-forms, numpy einsum).
+forms, numpy einsum; the weight gradient against numpy einsum, the adjoint
+identity with the einsum and the linearity of the fused forward in W).
 """
 from __future__ import annotations
 
@@ -74,6 +75,8 @@ def _load():
         lib.oracle_einsum.argtypes = [P, i32, i32, i32, i64, i32, P, P, P, P]
         lib.oracle_einsum_t.restype = None
         lib.oracle_einsum_t.argtypes = [P, i32, i32, i32, i64, i32, P, P, P]
+        lib.oracle_einsum_w.restype = None
+        lib.oracle_einsum_w.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P]
         lib.oracle_fwd_points.restype = None
         lib.oracle_fwd_points.argtypes = [P, P, P] + shape + [P, i64, P, P, P]
         lib.oracle_bwd_points.restype = None
@@ -259,6 +262,27 @@ def einsum_t(W, dy):
     SdX = np.empty_like(dX)
     _load().oracle_einsum_t(_p(W), Cout, Cin, K, P, B, _p(dy), _p(dX), _p(SdX))
     return dX, SdX
+
+
+def einsum_w(dy, X, SX=None):
+    """dy[B, Cout, Hout, Wout], X[B, Cin, K, Hout, Wout] -> (dW[Cout, Cin, K], SdW):
+    the weight gradient of y = einsum(W, X), dW[o,c,k] = sum_{b,p} dy[b,o,p] X[b,c,k,p]."""
+    dy, X = _f64(dy), _f64(X)
+    B, Cout = dy.shape[:2]
+    Cin, K = X.shape[1], X.shape[2]
+    P = dy.shape[2] * dy.shape[3]
+    dW = np.empty((Cout, Cin, K), np.float64)
+    SdW = np.empty_like(dW)
+    sx = _f64(SX) if SX is not None else None
+    _load().oracle_einsum_w(_p(dy), _p(X), _p(sx) if sx is not None else None, Cout, Cin, K, P, B,
+                            _p(dW), _p(SdW))
+    return dW, SdW
+
+
+def fused_bwd_weight(psi: OraclePsi, x, dy):
+    """Weight gradient of the fused forward: dW = sum_{b,p} dy * fwd(x)."""
+    X, SX = fwd(psi, x)
+    return einsum_w(dy, X, SX)
 
 
 def fused(psi: OraclePsi, x, W):

@@ -415,6 +415,30 @@ void oracle_einsum_t(const double* W, int32_t Cout, int32_t Cin, int32_t K,
       }
 }
 
+/* Weight gradient of the fused forward (the einsum's other adjoint):
+   dW[o,c,k] = sum_b sum_p dy[b,o,p] X[b,c,k,p];  SdW = sum |dy| SX.
+   X is the forward contraction of x, SX its sum of |terms|. */
+void oracle_einsum_w(const double* dy, const double* X, const double* SX, int32_t Cout,
+                     int32_t Cin, int32_t K, int64_t P, int32_t B, double* dW, double* SdW) {
+#pragma omp parallel for collapse(3) schedule(static)
+  for (int32_t o = 0; o < Cout; ++o)
+    for (int32_t c = 0; c < Cin; ++c)
+      for (int32_t k = 0; k < K; ++k) {
+        double acc = 0.0, sacc = 0.0;
+        for (int32_t b = 0; b < B; ++b) {
+          const double* dp = dy + ((int64_t)b * Cout + o) * P;
+          const double* xp = X + (((int64_t)b * Cin + c) * K + k) * P;
+          const double* xs = SX ? SX + (((int64_t)b * Cin + c) * K + k) * P : NULL;
+          for (int64_t p = 0; p < P; ++p) {
+            acc += dp[p] * xp[p];
+            sacc += fabs(dp[p]) * (xs ? xs[p] : fabs(xp[p]));
+          }
+        }
+        dW[((int64_t)o * Cin + c) * K + k] = acc;
+        if (SdW) SdW[((int64_t)o * Cin + c) * K + k] = sacc;
+      }
+}
+
 /* ------------------------------------------------------ sampled points -- */
 /* The sampled forms read their inputs from fp32 storage (every bf16 or fp32
    input value is exactly representable there) and compute in fp64. */

@@ -294,6 +294,45 @@ def test_einsum_against_numpy():
     assert np.abs(dX - np.einsum("ock,bohw->bckhw", W, dy)).max() < 1e-12
 
 
+def test_weight_gradient_against_numpy_and_adjoint():
+    """dW of y = einsum(W, X): against numpy.einsum, and the adjoint identity
+    <dW, V> = <dy, einsum(V, X)> with the (independently pinned) einsum."""
+    rng = np.random.default_rng(15)
+    B, Cin, K, Cout = 2, 4, 9, 6
+    X = rng.standard_normal((B, Cin, K, 3, 5))
+    dy = rng.standard_normal((B, Cout, 3, 5))
+    dW, SdW = oracle.einsum_w(dy, X)
+    assert np.abs(dW - np.einsum("bohw,bckhw->ock", dy, X)).max() < 1e-12
+    assert np.abs(SdW - np.einsum("bohw,bckhw->ock", np.abs(dy), np.abs(X))).max() < 1e-12
+    V = rng.standard_normal((Cout, Cin, K))
+    y, _ = oracle.einsum(V, X)
+    lhs, rhs = float(np.sum(dW * V)), float(np.sum(dy * y))
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(rhs))
+    # a transposed operand (c and k swapped in X) breaks the identity
+    Xt = np.ascontiguousarray(X.reshape(B, K, Cin, 3, 5).transpose(0, 2, 1, 3, 4))
+    dWt, _ = oracle.einsum_w(dy, Xt)
+    assert abs(float(np.sum(dWt * V)) - rhs) > 1e-6 * max(1.0, abs(rhs))
+
+
+@pytest.mark.parametrize("case", TINY[:2], ids=lambda c: f"{c[0]}->{c[1]}")
+def test_fused_weight_gradient_is_the_derivative(case):
+    """The fused forward is linear in W, so <dy, y(W + V)> - <dy, y(W)> equals
+    <dW, V> exactly (up to rounding), with dW from fused_bwd_weight."""
+    gi, go, kind, nrad, cut = case
+    psi = oracle.build_psi(gi, go, kind, nrad, cut)
+    rng = np.random.default_rng(16)
+    B, C, Cout = 2, 3, 4
+    x = rng.standard_normal((B, C, gi[0], gi[1]))
+    dy = rng.standard_normal((B, Cout, go[0], go[1]))
+    W = rng.standard_normal((Cout, C, psi.K))
+    V = rng.standard_normal((Cout, C, psi.K))
+    dW, _ = oracle.fused_bwd_weight(psi, x, dy)
+    y0, _ = oracle.fused(psi, x, W)
+    y1, _ = oracle.fused(psi, x, W + V)
+    lhs, rhs = float(np.sum(dy * (y1 - y0))), float(np.sum(dW * V))
+    assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(rhs))
+
+
 @pytest.mark.parametrize("case", TINY[:4], ids=lambda c: f"{c[0]}->{c[1]}")
 def test_sampled_points_match_full_arrays(case):
     gi, go, kind, nrad, cut = case
