@@ -205,6 +205,23 @@ def run_ours(args):
     if d.disco_device_status() != 0:
         raise RuntimeError("a bounded wait timed out during the timed region")
 
+    # the weight gradient (a scope extension, not part of the step): timed alone
+    dw_ms = None
+    nwb = d.disco_fused_conv_bwd_weight_workspace_bytes(psi.c, B, C, Co) if Co is not None else 0
+    if nwb > 0:
+        wsw = torch.empty(nwb, dtype=torch.uint8, device=dev)
+        dW = torch.empty(sh["W"], dtype=dt, device=dev)
+        for _ in range(2):
+            d.disco_fused_conv_bwd_weight(psi.c, x, dy, dW, B, C, Co, wsw, stream)
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for _ in range(5):
+            d.disco_fused_conv_bwd_weight(psi.c, x, dy, dW, B, C, Co, wsw, stream)
+        q1.record(stream)
+        torch.cuda.synchronize()
+        dw_ms = q0.elapsed_time(q1) / 5
+        del wsw, dW
+
     # end to end through the C ABI with host buffers: pinned inputs in,
     # results out, copies inside the timed region
     e2e = None
@@ -276,6 +293,7 @@ def run_ours(args):
         "hbm_frac_of_measured_peak": round(value / ws / peaks["hbm_gbs"], 4),
         "fused_conv_ms_per_call": round(med["fused"], 3),
         "fused_conv_bwd_input_ms_per_call": round(med["fused_bwd"], 3),
+        "fused_conv_bwd_weight_ms_per_call": round(dw_ms, 3) if dw_ms is not None else None,
         "kernel_ms": {k: round(v, 3) for k, v in med.items()},
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",

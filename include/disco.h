@@ -281,6 +281,31 @@ DISCO_API int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const voi
                                                  int32_t Cin, int32_t Cout, disco_dtype dtype,
                                                  void* stream);
 
+/* Device workspace bytes of disco_fused_conv_bwd_weight: X (bf16) plus the
+   fp32 partial sums of the split reduction; 0 when the call does not take the
+   shape (see below). */
+DISCO_API size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* psi, int32_t B,
+                                                            int32_t Cin, int32_t Cout, disco_dtype dtype);
+
+/* Weight gradient of the fused convolution (§Architecture snapshot: the
+   fused variants are paired with their backward through autograd functions;
+   the page gives no formula, the plain reading is the gradient of
+   y = einsum(W, X) with respect to W):
+     dW[o,c,k] = sum_b sum_{ho,wo} dy[b,o,ho,wo] X[b,c,k,ho,wo],
+   X the forward contraction of x (recomputed, not stored by the forward).
+   x: [B, Cin, H_in, W_in], dy: [B, Cout, H_out, W_out], dW: [Cout, Cin, K],
+   all bf16 (dW rounded from an fp32 sum).  X is built by the tensor-core
+   contraction into `workspace` (>= disco_fused_conv_bwd_weight_workspace_bytes,
+   256-byte aligned), then a tcgen05 GEMM over the pixels (reduction split
+   across CTAs into fp32 partials, summed in a fixed order: deterministic).
+   Takes bf16 with the tensor-core forward shape (W_in % 8 == 0, W_in >= 64,
+   s in {1, 2}, K <= 9), H_out*W_out, Cin*K and Cout multiples of 8,
+   Cin*K >= 64 and Cout >= 16; else DISCO_ERR_UNSUPPORTED.  Asynchronous on
+   `stream`. */
+DISCO_API int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, const void* dy, void* dW,
+                                          int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,

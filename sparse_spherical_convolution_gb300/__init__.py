@@ -20,7 +20,8 @@ __all__ = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
-    "disco_fused_conv_bwd_input_noalloc", "disco_device_status", "library_path",
+    "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
+    "disco_fused_conv_bwd_weight", "disco_device_status", "library_path",
     "load_library", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -32,7 +33,8 @@ EXPORTED_SYMBOLS = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_fwd", "disco_bwd", "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
-    "disco_fused_conv_bwd_input_noalloc", "disco_device_status",
+    "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
+    "disco_fused_conv_bwd_weight", "disco_device_status",
 ]
 
 
@@ -111,6 +113,10 @@ def load_library():
     lib.disco_fused_conv_bwd_input.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_fused_conv_bwd_input_noalloc.restype = ctypes.c_int
     lib.disco_fused_conv_bwd_input_noalloc.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P]
+    lib.disco_fused_conv_bwd_weight_workspace_bytes.restype = SZ
+    lib.disco_fused_conv_bwd_weight_workspace_bytes.argtypes = [PP, I32, I32, I32, ctypes.c_int]
+    lib.disco_fused_conv_bwd_weight.restype = ctypes.c_int
+    lib.disco_fused_conv_bwd_weight.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_device_status.restype = ctypes.c_int
     lib.disco_device_status.argtypes = [ctypes.POINTER(I32), I32]
     _lib = lib
@@ -220,6 +226,19 @@ def disco_fused_conv_bwd_input(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout
                                workspace, stream=None) -> None:
     _check(load_library().disco_fused_conv_bwd_input(
         ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy),
+        _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
+        _stream(stream)))
+
+
+def disco_fused_conv_bwd_weight_workspace_bytes(psi: disco_psi, B: int, Cin: int, Cout: int,
+                                                 dtype=DISCO_BF16) -> int:
+    return load_library().disco_fused_conv_bwd_weight_workspace_bytes(ctypes.byref(psi), B, Cin, Cout, dtype)
+
+
+def disco_fused_conv_bwd_weight(psi: disco_psi, x, dy, dW, B: int, Cin: int, Cout: int,
+                                workspace, stream=None) -> None:
+    _check(load_library().disco_fused_conv_bwd_weight(
+        ctypes.byref(psi), _ptr(x), _ptr(dy), _ptr(dW), B, Cin, Cout, _dtype(x),
         _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
         _stream(stream)))
 

@@ -719,6 +719,40 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   return disco_bwd(psi, workspace, gx, B, Cin, dtype, stream);
 }
 
+static size_t align256z(size_t v) { return (v + 255) & ~(size_t)255; }
+
+extern "C" size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
+                                                              int32_t Cout, disco_dtype dtype) {
+  if (!psi || B < 1 || Cin < 1 || Cout < 1 || dtype != DISCO_BF16 || !fwd_tc_supported(psi, B * Cin))
+    return 0;
+  const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
+  const int CK = Cin * psi->K;
+  if (!dw_tensor_core_supported(B, Cout, CK, P)) return 0;
+  return align256z((size_t)B * CK * P * 2) + dw_partial_bytes(B, Cout, CK, P);
+}
+
+extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, const void* dy, void* dW,
+                                           int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_fused_common(psi, x, dy, dW, B, Cin, Cout, dtype);
+  if (st) return st;
+  const size_t need = disco_fused_conv_bwd_weight_workspace_bytes(psi, B, Cin, Cout, dtype);
+  if (need == 0)
+    return fail(DISCO_ERR_UNSUPPORTED,
+                "weight gradient: needs the tensor-core forward shape (bf16, W_in % 8 == 0, W_in >= 64, "
+                "K <= 9) with H_out*W_out, Cin*K and Cout multiples of 8, Cin*K >= 64, Cout >= 16");
+  if (!workspace || workspace_bytes < need) return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(DISCO_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
+  const int CK = Cin * psi->K;
+  // X = the forward contraction (bf16) in the first part of the workspace
+  if ((st = fwd_tensor_core(psi, x, workspace, B * Cin, s))) return st;
+  void* part = (char*)workspace + align256z((size_t)B * CK * P * 2);
+  return dw_tensor_core(dy, workspace, dW, part, B, Cout, CK, P, s);
+}
+
 extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
   if (!flags) return fail(DISCO_ERR_INVALID_ARG, "flags is null");
   int st = check_device();

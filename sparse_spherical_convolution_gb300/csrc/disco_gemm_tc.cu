@@ -90,6 +90,7 @@ __host__ __device__ constexpr uint32_t idesc_mn(int M, int N, bool b_mn) {
 
 struct GemmTcArgs {
   __nv_bfloat16* out;  // [B][Nt][P]
+  uint32_t bbytes;     // bytes of the B boxes of one stage
   int64_t P;           // pixels
   int Kt;              // reduction length j
   int Nt;              // outputs n
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = a.mt * a.nt * a.B;
   const int nk = (a.Kt + kBK - 1) / kBK;
-  const uint32_t bbytes = (uint32_t)a.NB * kBK * 2;
+  const uint32_t bbytes = a.bbytes;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -274,6 +275,196 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------- dW = sum_p dy X^T --
+//
+// Weight gradient of the fused convolution, y = einsum(W, X):
+//   dW[o, n] = sum_b sum_p dy[b, o, p] X[b, n, p]          (n = c*K + k)
+// Both operands are K-major with the pixels as the reduction (dy rows o, X
+// rows n, pixels contiguous), one TMA box each per 64 pixels.  Tiles of 128 o
+// x NB n; the reduction over (b, pixel chunks) is split across CTAs
+// (deterministic: each split writes fp32 partial sums, a second kernel adds
+// them in split order and rounds to bf16).
+
+struct DwArgs {
+  float* part;         // [nsplit][mt*128][nt*NB] fp32 partial sums
+  uint32_t abytes, bbytes;  // bytes of one A / B box (rows clipped to the tensor)
+  int64_t P;
+  int Cout, Nt, NB;    // rows o, columns n, columns per tile
+  int mt, nt, nsplit;  // tiles along o, along n, reduction splits
+  int nkp, B;          // 64-pixel chunks per image, images
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dw_gemm_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                   const DwArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kEpiStage);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* accf = bars + 2 * kStages;
+  uint64_t* acce = bars + 2 * kStages + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = a.mt * a.nt * a.nsplit;
+  const int nq = a.nkp * a.B;  // (image, pixel chunk) reduction steps
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiThreads);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // tile t: split fastest, then n, then o; split sp reduces steps [q0, q1)
+  auto coords = [&](int t, int* o0, int* n0, int* sp, int* q0, int* q1) {
+    *sp = t % a.nsplit;
+    const int r = t / a.nsplit;
+    *n0 = (r % a.nt) * a.NB;
+    *o0 = (r / a.nt) * kBM;
+    *q0 = (int)((long long)nq * *sp / a.nsplit);
+    *q1 = (int)((long long)nq * (*sp + 1) / a.nsplit);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int o0, n0, sp, q0, q1;
+        coords(t, &o0, &n0, &sp, &q0, &q1);
+        for (int q = q0; q < q1; ++q, ++i) {
+          const int s = i % kStages;
+          if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          const int b = q / a.nkp, p0 = (q - b * a.nkp) * kBK;
+          uint8_t* sa = smem + s * kStageBytes;
+          // rows of a box past the tensor (o >= Cout, n >= Nt) keep stale values:
+          // they only reach accumulator rows / columns that are never reduced
+          mbar_expect_tx(&full[s], a.abytes + a.bbytes);
+          tma_load_3d(sa, &amap, p0, o0, b, &full[s]);
+          tma_load_3d(sa + kABytes, &bmap, p0, n0, b, &full[s]);
+        }
+      }
+      if (!ok) {
+        gemm_flag();
+        *abort_flag = 1;
+        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
+          const int li = i - back;
+          mbar_wait(&full[li % kStages], (li / kStages) & 1, kWaitLimit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, a.NB);
+      int i = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+        int o0, n0, sp, q0, q1;
+        coords(t, &o0, &n0, &sp, &q0, &q1);
+        const int ab = tl & 1;
+        if (tl >= 2 && !mbar_wait(&acce[ab], ((tl >> 1) - 1) & 1, kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + ab * 256;
+        for (int q = q0; q < q1; ++q, ++i) {
+          const int s = i % kStages;
+          if (!mbar_wait(&full[s], (i / kStages) & 1, kWaitLimit) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks)
+            umma_bf16(d, desc_sw128(sa + ks * 32, 16, 1024), desc_sw128(sb + ks * 32, 16, 1024), idesc,
+                      (q > q0 || ks > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&accf[ab]);
+      }
+      if (!ok) {
+        gemm_flag();
+        *abort_flag = 1;
+        if (i > 0) mbar_wait(&empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, kWaitLimit);
+      }
+    }
+  } else {
+    const int q4 = warp & 3;
+    int tl = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+      const int ab = tl & 1;
+      bool fin = mbar_wait(&accf[ab], (tl >> 1) & 1, kWaitLimit);
+      fin = __all_sync(0xffffffffu, fin) && !*abort_flag;
+      if (!fin) {
+        if (lane == 0) gemm_flag();
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      int o0, n0, sp, q0, q1;
+      coords(t, &o0, &n0, &sp, &q0, &q1);
+      const bool empty_split = q1 <= q0;  // no reduction steps: the partial is zero
+      const int row = o0 + q4 * 32 + lane;
+      float* dst = a.part + ((size_t)sp * a.mt * kBM + row) * ((size_t)a.nt * a.NB) + n0;
+      for (int c0 = 0; c0 < a.NB; c0 += 16) {
+        float v[16];
+        if (!empty_split) {
+          tmem_ld16(tmem + ab * 256 + ((uint32_t)(q4 * 32) << 16) + c0, v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          reinterpret_cast<float4*>(dst + c0)[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(&acce[ab]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dW[o][n] = bf16(sum over splits, in split order, of the partials)
+__global__ void dw_reduce_kernel(const float* part, __nv_bfloat16* dW, int Cout, int Nt, int rows, int cols,
+                                 int nsplit) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)Cout * Nt) return;
+  const int o = (int)(i / Nt), n = (int)(i - (int64_t)o * Nt);
+  float acc = 0.f;
+  for (int sp = 0; sp < nsplit; ++sp) acc += part[((size_t)sp * rows + o) * cols + n];
+  dW[i] = __float2bfloat16_rn(acc);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -324,6 +515,8 @@ int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, 
   g.mt = (int)((P + kBM - 1) / kBM);
   g.nt = (Nt + g.NB - 1) / g.NB;
   g.B = B;
+  // K-major B rows past Nt are not loaded (stale smem feeds only unstored columns)
+  g.bbytes = kBMN ? (uint32_t)g.NB * kBK * 2 : (uint32_t)(Nt < g.NB ? Nt : g.NB) * kBK * 2;
   CUtensorMap amap, bmap;
   {
     cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)Kt, (cuuint64_t)B};
@@ -335,7 +528,7 @@ int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, 
   {
     cuuint64_t dims[2] = {kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt, kBMN ? (cuuint64_t)Kt : (cuuint64_t)Nt};
     cuuint64_t strides[1] = {(kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt) * 2};
-    cuuint32_t box[2] = {64, kBMN ? (cuuint32_t)kBK : (cuuint32_t)g.NB};
+    cuuint32_t box[2] = {64, kBMN ? (cuuint32_t)kBK : (cuuint32_t)(Nt < g.NB ? Nt : g.NB)};
     int s = encode(&bmap, W, 2, dims, strides, box);
     if (s) return s;
   }
@@ -363,6 +556,81 @@ int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P, cudaStream_t st) {
   if (!gemm_tc_supported(P, Cout, CK) || CK % 64 != 0) return DISCO_ERR_UNSUPPORTED;
   return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st);
+}
+
+namespace {
+struct DwPlan {
+  int mt, nt, NB, nsplit, nkp;
+};
+DwPlan dw_plan(int B, int Cout, int CK, int64_t P) {
+  DwPlan d;
+  d.NB = CK >= 256 ? 256 : (CK + 15) / 16 * 16;
+  d.mt = (Cout + kBM - 1) / kBM;
+  d.nt = (CK + d.NB - 1) / d.NB;
+  d.nkp = (int)((P + kBK - 1) / kBK);
+  const long long steps = (long long)d.nkp * B;
+  long long ns = (2LL * sm_count_g() + (long long)d.mt * d.nt - 1) / ((long long)d.mt * d.nt);
+  if (ns > steps) ns = steps;
+  if (ns < 1) ns = 1;
+  d.nsplit = (int)ns;
+  return d;
+}
+}  // namespace
+
+bool dw_tensor_core_supported(int B, int Cout, int CK, int64_t P) {
+  return B >= 1 && gemm_tc_supported(P, CK, Cout) && Cout >= 16 && CK >= 16;
+}
+
+size_t dw_partial_bytes(int B, int Cout, int CK, int64_t P) {
+  const DwPlan d = dw_plan(B, Cout, CK, P);
+  return (size_t)d.nsplit * d.mt * kBM * ((size_t)d.nt * d.NB) * 4;
+}
+
+int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int B, int Cout, int CK, int64_t P,
+                   cudaStream_t st) {
+  if (!dw_tensor_core_supported(B, Cout, CK, P)) return DISCO_ERR_UNSUPPORTED;
+  const DwPlan d = dw_plan(B, Cout, CK, P);
+  DwArgs g;
+  g.part = (float*)partials;
+  g.P = P;
+  g.Cout = Cout;
+  g.Nt = CK;
+  g.NB = d.NB;
+  g.mt = d.mt;
+  g.nt = d.nt;
+  g.nsplit = d.nsplit;
+  g.nkp = d.nkp;
+  g.B = B;
+  const int arows = Cout < kBM ? Cout : kBM, brows = CK < d.NB ? CK : d.NB;
+  g.abytes = (uint32_t)arows * kBK * 2;
+  g.bbytes = (uint32_t)brows * kBK * 2;
+  CUtensorMap amap, bmap;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)Cout, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)Cout * P * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)arows, 1};
+    int s = encode(&amap, dy, 3, dims, strides, box);
+    if (s) return s;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)CK, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)CK * P * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)brows, 1};
+    int s = encode(&bmap, X, 3, dims, strides, box);
+    if (s) return s;
+  }
+  if (cudaFuncSetAttribute(dw_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
+      cudaSuccess)
+    return check_launch("dW GEMM attribute");
+  const long long ntiles = (long long)d.mt * d.nt * d.nsplit;
+  const int grid = (int)(ntiles < sm_count_g() ? ntiles : sm_count_g());
+  dw_gemm_kernel<<<grid, kThreads, kSmem, st>>>(amap, bmap, g);
+  int s = check_launch("dW GEMM");
+  if (s) return s;
+  const long long n = (long long)Cout * CK;
+  dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
+      (const float*)partials, (__nv_bfloat16*)dW, Cout, CK, d.mt * kBM, d.nt * d.NB, d.nsplit);
+  return check_launch("dW reduce");
 }
 
 cudaError_t gemm_status(int32_t* v, bool clear) {

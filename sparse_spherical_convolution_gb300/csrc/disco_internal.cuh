@@ -46,6 +46,12 @@ int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P,
                    cudaStream_t st);
 cudaError_t gemm_status(int32_t* v, bool clear);
+// Weight gradient dW[o][j] = sum_b sum_p dy[b][o][p] X[b][j][p] (split reduction
+// through fp32 partials of dw_partial_bytes bytes, then rounded to bf16).
+bool dw_tensor_core_supported(int B, int Cout, int CK, int64_t P);
+size_t dw_partial_bytes(int B, int Cout, int CK, int64_t P);
+int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int B, int Cout, int CK, int64_t P,
+                   cudaStream_t st);
 
 // Geometry of the transpose tables by input-row group (disco_psi.grp_ptr):
 // 8 input rows per group, 64-column chunks, TQ = 32 / s decimated output
