@@ -452,6 +452,340 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------- persistent form --
+//
+// The same tiles, items and operands, but one CTA per SM walks the tiles
+// (output row in launch order, 128 channels, NT*16 columns) round-robin and
+// its pipeline runs across tile boundaries: the next tile's x windows and
+// psi tables load and its T chunks build while the epilogue writes the
+// previous tile.  The epilogue has its own warps (8-11) and writes X one
+// basis function at a time ([128 channels x NT*16 columns]) through a
+// two-piece shared-memory ring with TMA stores.  The accumulators (NT*N <=
+// 512 columns) are single-buffered: a tile's first MMA waits for the
+// epilogue to have read the previous tile out.
+constexpr int kPThreads = 384;
+constexpr int kPEpiThreads = 128;  // warps 8-11
+
+template <int K, int S>
+struct PCfg {
+  using C = TcCfg<K, S, 3>;
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kPiece = 128 * C::kOutRow;  // one basis function of a tile
+  static size_t smem(int TLB) {
+    return (size_t)kStages * C::kStageBytes + 2 * C::tab_bytes(TLB) + 2 * kPiece + 256 + 1024;
+  }
+};
+
+template <int K, int S>
+__global__ void __launch_bounds__(kPThreads, 1)
+    fwd_tcp_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xnarrow,
+                   const __grid_constant__ CUtensorMap outmap, const TcArgs a) {
+  using Cfg = TcCfg<K, S, 3>;
+  using P = PCfg<K, S>;
+  constexpr int STAGES = P::kStages;
+  constexpr int N = Cfg::N, NT = Cfg::NT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const size_t tab_bytes = Cfg::tab_bytes(a.TLB);
+  uint8_t* tabs = smem + STAGES * Cfg::kStageBytes;          // [2] run tables
+  uint8_t* pieces = tabs + 2 * tab_bytes;                     // [2] X pieces for the TMA stores
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pieces + 2 * P::kPiece);
+  uint64_t* fullA = bars;                    // [STAGES]
+  uint64_t* fullB = bars + STAGES;           // [STAGES] (192 arrivals)
+  uint64_t* empty = bars + 2 * STAGES;       // [STAGES] (commit)
+  uint64_t* tfull = bars + 3 * STAGES;       // [2] run table landed
+  uint64_t* tempty = bars + 3 * STAGES + 2;  // [2] run table released (192 arrivals)
+  uint64_t* acc_full = bars + 3 * STAGES + 4;   // tile's MMAs done (commit)
+  uint64_t* tmem_empty = bars + 3 * STAGES + 5; // epilogue read the tile out (128 arrivals)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 7);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntx = (a.Wout + kTW * NT - 1) / (kTW * NT), nty = (a.BC + 127) / 128;
+  const int ntiles = ntx * nty * a.Hout;
+  auto coords = [&](int t, int* ho, int* bc0, int* wc) {
+    *wc = (t % ntx) * (kTW * NT);
+    const int r = t / ntx;
+    *bc0 = (r % nty) * 128;
+    *ho = a.row_order[r / nty];
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&fullA[s], 1);
+      mbar_init(&fullB[s], kBuilderThreads);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kBuilderThreads);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(tmem_empty, kPEpiThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, Cfg::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int i = 0, rl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int ho, bc0, wc;
+        coords(t, &ho, &bc0, &wc);
+        const int r_end = a.run_ptr[ho + 1];
+        for (int r = a.run_ptr[ho]; r < r_end && ok; ++r, ++rl) {
+          const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+          const int u0 = S * wc - g.M;
+          const int b = rl & 1;
+          if ((rl >= 2 && !mbar_wait(&tempty[b], ((rl >> 1) - 1) & 1, kWaitLimit)) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = (uint32_t)K * g.TL * 2;
+          mbar_expect_tx(&tfull[b], bytes);
+          bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+          for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+            const int s = i % STAGES;
+            if ((i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitLimit)) || *abort_flag) {
+              ok = false;  // (the r loop's increment still counts this run's table copy)
+              break;
+            }
+            const int nks = min(kCK, g.KS - c * kCK);
+            const int nbox = (16 * nks + S * kTW * (NT - 1) + 63) / 64;
+            uint8_t* sA = smem + s * Cfg::kStageBytes;
+            mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
+            for (int bb = 0; bb < nbox; ++bb) {
+              const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
+              if (col + 64 <= a.Win) {
+                tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+              } else {
+                for (int gi = 0; gi < 8; ++gi)
+                  tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow, wrap_col(col + 8 * gi, a.Win),
+                              g.hi, bc0, &fullA[s]);
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        tc_flag(kStatusTcTimeout);
+        *abort_flag = 1;
+        for (int back = 1; back <= STAGES && i - back >= 0; ++back) {
+          const int li = i - back;
+          mbar_wait(&fullA[li % STAGES], (li / STAGES) & 1, kWaitLimit);
+        }
+        for (int back = 1; back <= 2 && rl - back >= 0; ++back) {
+          const int lr = rl - back;
+          mbar_wait(&tfull[lr & 1], (lr >> 1) & 1, kWaitLimit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, N);
+      int i = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+        int ho, bc0, wc;
+        coords(t, &ho, &bc0, &wc);
+        if ((tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        bool first = true;
+        const int r_end = a.run_ptr[ho + 1];
+        for (int r = a.run_ptr[ho]; r < r_end && ok; ++r) {
+          const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+          for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+            const int s = i % STAGES;
+            const uint32_t ph = (i / STAGES) & 1;
+            if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int nks = min(kCK, g.KS - c * kCK);
+            const uint32_t abase = smem_u32(smem + s * Cfg::kStageBytes);
+            const uint32_t bbase = abase + Cfg::kABytes;
+            const int u0 = S * wc - g.M;
+            bool narrow[Cfg::NBOX];
+#pragma unroll
+            for (int bb = 0; bb < Cfg::NBOX; ++bb)
+              narrow[bb] = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win) + 64 > a.Win;
+            for (int j = 0; j < NT; ++j)
+              for (int ks = 0; ks < nks; ++ks) {
+                const int col = 16 * ks + S * kTW * j;
+                const int bb = col >> 6, ka = (col & 63) >> 4;
+                bool nb = false;
+#pragma unroll
+                for (int q = 0; q < Cfg::NBOX; ++q)
+                  if (q == bb) nb = narrow[q];
+                const uint32_t slot = abase + bb * kBoxBytes;
+                const uint64_t ad = nb ? smem_desc(slot + ka * 2 * kNarrowBytes, kNarrowBytes, 128)
+                                       : smem_desc_sw128(slot + 32 * ka);
+                const uint64_t bd = smem_desc_sw128(bbase + 32 * ks);
+                umma_bf16(tmem + j * N, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
+              }
+            first = false;
+            umma_commit(&empty[s]);
+          }
+        }
+        if (!ok) break;
+        // a tile without runs leaves the accumulators unwritten: the epilogue stores zeros
+        umma_commit(acc_full);
+      }
+      if (!ok) {
+        tc_flag(kStatusTcTimeout);
+        *abort_flag = 1;
+        if (i > 0) mbar_wait(&empty[(i - 1) % STAGES], ((i - 1) / STAGES) & 1, kWaitLimit);
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------- B builders (6 warps) --
+    const int btid = tid - 64;
+    int i = 0, rl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      int ho, bc0, wc;
+      coords(t, &ho, &bc0, &wc);
+      const int r_end = a.run_ptr[ho + 1];
+      for (int r = a.run_ptr[ho]; r < r_end && ok; ++r, ++rl) {
+        const RunGeom g = run_geom<S>(a.runs[r], a.Win);
+        const int tb = rl & 1;
+        const uint16_t* tab = reinterpret_cast<const uint16_t*>(tabs + tb * tab_bytes);
+        {
+          const bool mine = mbar_wait(&tfull[tb], (rl >> 1) & 1, kWaitLimit) && !*abort_flag;
+          ok = group_all_b(mine, 1, kBuilderThreads);
+          if (!ok) break;
+        }
+        for (int c = 0; c * kCK < g.KS; ++c, ++i) {
+          const int s = i % STAGES;
+          bool mine = true;
+          if (i >= STAGES) mine = mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitLimit);
+          ok = group_all_b(mine && !*abort_flag, 1, kBuilderThreads);
+          if (!ok) break;
+          uint8_t* sB = smem + s * Cfg::kStageBytes + Cfg::kABytes;
+          const int nks = min(kCK, g.KS - c * kCK);
+          const int ngrp = 2 * nks;
+          for (int idx = btid; idx < N * ngrp; idx += kBuilderThreads) {
+            const int n = idx % N, gi = idx / N;
+            const int k = n >> 4, tt = n & 15;
+            const int x0 = 8 + c * kChunkCols + 8 * gi - S * tt - g.M - g.dlo;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (x0 + 7 >= 0 && x0 < g.TL) {
+              const uint16_t* row = tab + (size_t)k * g.TL;
+              uint16_t v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int x = x0 + e;
+                v[e] = (x >= 0 && x < g.TL) ? row[x] : (uint16_t)0;
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) w[e] = (uint32_t)v[2 * e] | ((uint32_t)v[2 * e + 1] << 16);
+            }
+            *reinterpret_cast<uint4*>(sB + n * 128 + ((gi ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&fullB[s]);
+        }
+        if (!ok) break;
+        mbar_arrive(&tempty[tb]);  // this run's table is no longer read
+      }
+    }
+    if (!ok) {
+      tc_flag(kStatusTcTimeout);
+      *abort_flag = 1;
+    }
+  } else {
+    // ---------------------------------------------- epilogue (warps 8-11) --
+    const int q = warp & 3;
+    const int er = q * 32 + lane;  // channel row of this thread in a piece
+    int tl = 0, npiece = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+      int ho, bc0, wc;
+      coords(t, &ho, &bc0, &wc);
+      const bool any = a.run_ptr[ho + 1] > a.run_ptr[ho];
+      bool fin = mbar_wait(acc_full, tl & 1, kWaitLimit) && !*abort_flag;
+      fin = group_all_b(fin, 2, kPEpiThreads);  // one decision for the 4 warps (named barriers below)
+      if (!fin) {
+        if (lane == 0) tc_flag(kStatusTcTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      for (int k = 0; k < K; ++k, ++npiece) {
+        uint8_t* pb = pieces + (npiece & 1) * P::kPiece;
+        if (tid == 256) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // buffer free
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        for (int j = 0; j < NT; ++j) {
+          float v[16];
+          if (any) {
+            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + j * N + k * 16, v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0.f;
+          }
+          uint32_t w32[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(pb + (size_t)er * Cfg::kOutRow + j * kTW * 2);
+          dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
+          dst[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
+        }
+        if (k == K - 1) {  // every accumulator read: the next tile's MMAs may start
+          tc_fence_before();
+          mbar_arrive(tmem_empty);
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (tid == 256) {
+          asm volatile(
+              "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                  reinterpret_cast<uint64_t>(&outmap)),
+              "r"(wc), "r"(k * a.Hout + ho), "r"(bc0), "r"(smem_u32(pb))
+              : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+    }
+    if (tid == 256) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+int sm_count_f() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 1;
+  }
+  return n;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -525,6 +859,18 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
     CUresult cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, X, od, os, ob, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
+  }
+  if (a.tma_store && PCfg<K, S>::smem(a.TLB) <= kMaxSmem) {
+    // persistent form: one CTA per SM over all tiles
+    const size_t smem = PCfg<K, S>::smem(a.TLB);
+    auto kern = fwd_tcp_kernel<K, S>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return check_launch("disco_fwd (tensor cores) attribute");
+    const long long ntiles = (long long)((a.Wout + kTW * NT3 - 1) / (kTW * NT3)) * ((BC + 127) / 128) * a.Hout;
+    if (ntiles > 0x7fffffffLL) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
+    const int grid = (int)(ntiles < sm_count_f() ? ntiles : sm_count_f());
+    kern<<<grid, kPThreads, smem, st>>>(map, nmap, omap, a);
+    return check_launch("disco_fwd (tensor cores)");
   }
   return fit3 ? launch_tc_stages<K, S, 3>(psi, map, nmap, omap, a, st)
               : launch_tc_stages<K, S, 2>(psi, map, nmap, omap, a, st);
