@@ -620,23 +620,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t abase = smem_u32(smem + s * Cfg::kStageBytes);
             const uint32_t bbase = abase + Cfg::kABytes;
             const int u0 = S * wc - g.M;
+            // descriptors of every (tile block, K step) first, then the MMAs back to back
+            uint64_t dbox[Cfg::NBOX];
             bool narrow[Cfg::NBOX];
 #pragma unroll
-            for (int bb = 0; bb < Cfg::NBOX; ++bb)
+            for (int bb = 0; bb < Cfg::NBOX; ++bb) {
               narrow[bb] = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win) + 64 > a.Win;
+              dbox[bb] = narrow[bb] ? smem_desc(abase + bb * kBoxBytes, kNarrowBytes, 128)
+                                    : smem_desc_sw128(abase + bb * kBoxBytes);
+            }
+            const uint64_t dB = smem_desc_sw128(bbase);
+            const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
             for (int j = 0; j < NT; ++j)
-              for (int ks = 0; ks < nks; ++ks) {
+#pragma unroll
+              for (int ks = 0; ks < kCK; ++ks) {
+                // window column of the K step inside the stage: its box and its step in the box
                 const int col = 16 * ks + S * kTW * j;
                 const int bb = col >> 6, ka = (col & 63) >> 4;
-                bool nb = false;
-#pragma unroll
-                for (int q = 0; q < Cfg::NBOX; ++q)
-                  if (q == bb) nb = narrow[q];
-                const uint32_t slot = abase + bb * kBoxBytes;
-                const uint64_t ad = nb ? smem_desc(slot + ka * 2 * kNarrowBytes, kNarrowBytes, 128)
-                                       : smem_desc_sw128(slot + 32 * ka);
-                const uint64_t bd = smem_desc_sw128(bbase + 32 * ks);
-                umma_bf16(tmem + j * N, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
+                const uint64_t ad = dbox[bb] + (uint64_t)(narrow[bb] ? ka * (2 * kNarrowBytes >> 4) : ka * 2);
+                if (ks < nks)
+                  umma_bf16(tmem + j * N, ad, dB + (uint64_t)(ks * 2), idesc, ks == 0 ? acc0 : 1u);
               }
             first = false;
             umma_commit(&empty[s]);
