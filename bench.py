@@ -287,7 +287,7 @@ def run_ours(args):
     # launch each, so their events time the kernel alone.  Bound: HBM, with
     # the algorithmic bytes of one launch (input + output + psi).
     dom = "bwd" if med["bwd"] >= med["fwd"] else "fwd"
-    dom_kernel = {"bwd": "bwd_tc_kernel", "fwd": "fwd_tc_kernel"}[dom]
+    dom_kernel = {"bwd": "bwd_tc_kernel", "fwd": "fwd_tcp_kernel"}[dom]
     dom_bytes = alg[dom + "_bytes"]
     achieved = dom_bytes / (med[dom] * 1e-3) / 1e9
     traffic = _traffic_from_profiles(dom_kernel, w.name)

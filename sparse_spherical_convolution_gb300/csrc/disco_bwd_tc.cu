@@ -31,10 +31,13 @@
 // unswizzled layout and read with that layout's descriptor); T is written in
 // the same swizzled layout by the builder warps.
 //
-// Persistent kernel: one CTA per SM walks the tiles round-robin, polar row
-// groups first; the pipeline runs across tile boundaries:
-//   warp 0      producer: per tile the group's entry list (bulk copy), per item
-//               (ho, k, chunk) the psi block (bulk copy) and 1-2 G boxes (TMA);
+// Persistent kernel: one CTA per SM; the producer takes the next tile from
+// the launch's scheduler counter (disco_sched.cuh), in an order that puts the
+// long polar row groups first and keeps the groups that share G rows close;
+// the pipeline runs across tile boundaries:
+//   warp 0      producer: per tile the tile index and the group's entry list
+//               (bulk copy) into one of two info slots, per item (ho, k,
+//               chunk) the psi block (bulk copy) and 1-2 G boxes (TMA);
 //   warp 1      MMA issuer (one thread);
 //   warps 2-7   build T;
 //   warps 8-11  epilogue: tcgen05.ld, bf16, 16-byte row stores.
@@ -43,11 +46,13 @@
 #include <cudaTypedefs.h>
 
 #include "disco_internal.cuh"
+#include "disco_sched.cuh"
 #include "disco_umma.cuh"
 
 namespace disco {
 
 __device__ int g_btc_status = 0;
+__device__ SchedSlot g_btc_sched[kSchedSlots];
 
 namespace {
 
@@ -110,6 +115,7 @@ struct BtcArgs {
   const uint16_t* gtab;
   int BC, Hin, Win, Hout, Wout, K;
   int ntx, nty, ntz;  // tiles along columns, channel blocks, row groups
+  unsigned long long launch_id;  // selects the scheduler slot
 };
 
 template <int S>
@@ -125,7 +131,8 @@ struct BCfg {
   static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kOutBytes + kInfoBytes + 256 + 1024;
 };
 
-// the z-th row group in processing order: poles first, then inwards
+// the z-th row group in processing order: poles first, then inwards, so the
+// tiles in flight cover two bands of adjacent groups (which share G rows)
 __device__ __forceinline__ int row_group(int z, int nz) { return (z & 1) ? nz - 1 - (z >> 1) : (z >> 1); }
 
 template <int S>
@@ -165,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 6);
   int32_t* info_cnt = reinterpret_cast<int32_t*>(bars + 3 * kStages + 7);  // [2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kStages + 8);
+  volatile int* tile_id = reinterpret_cast<volatile int*>(bars + 3 * kStages + 9);  // [2], -1 = no more tiles
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = a.ntx * a.nty * a.ntz;
@@ -198,14 +206,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int i = 0, tl = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
-        int qb, bc0, zg;
-        tile_coords<S>(a, tile, &qb, &bc0, &zg);
+      SchedSlot* slot = sched_claim(g_btc_sched, a.launch_id, kWaitLimit);
+      if (!slot) btc_flag(kStatusBtcTimeout);  // this CTA takes no tile
+      for (; ok; ++tl) {
         const int b = tl & 1;
         if ((tl >= 2 && !mbar_wait(&info_empty[b], ((tl >> 1) - 1) & 1, kWaitLimit)) || *abort_flag) {
           ok = false;
           break;
         }
+        const int tile = slot ? sched_next(slot) : ntiles;
+        if (tile >= ntiles) {  // tell the other roles to stop
+          tile_id[b] = -1;
+          info_cnt[b] = 0;
+          mbar_arrive(&info_full[b]);
+          break;
+        }
+        tile_id[b] = tile;
+        int qb, bc0, zg;
+        tile_coords<S>(a, tile, &qb, &bc0, &zg);
         const int e0 = a.grp_ptr[zg];
         const int ne = min(a.grp_ptr[zg + 1] - e0, kMaxEnt);
         info_cnt[b] = ne;
@@ -261,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
         }
       }
+      if (slot) sched_release(slot);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
@@ -268,15 +287,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, kN);
       int i = 0, tl = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
-        int qb, bc0, zg;
-        tile_coords<S>(a, tile, &qb, &bc0, &zg);
+      for (; ok; ++tl) {
         const int b = tl & 1;
-        if (!mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) ||
-            (tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
+        if (!mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) || *abort_flag) {
           ok = false;
           break;
         }
+        const int tile = tile_id[b];
+        if (tile < 0) break;
+        if ((tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        int qb, bc0, zg;
+        tile_coords<S>(a, tile, &qb, &bc0, &zg);
         tc_fence_after();
         const int ne = info_cnt[b];
         const disco_grp_ent* info = infos + b * kMaxEnt;
@@ -331,13 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int btid = tid - 64;
     int i = 0, tl = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++tl) {
+    for (; ok; ++tl) {
       const int b = tl & 1;
       {
         const bool mine = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) && !*abort_flag;
         ok = all_named(mine, 1, kBuilderThreads);
         if (!ok) break;
       }
+      if (tile_id[b] < 0) break;  // same value for all builder threads
       const int ne = info_cnt[b];
       const disco_grp_ent* info = infos + b * kMaxEnt;
       for (int j = 0; j < ne && ok; ++j) {
@@ -378,12 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------- epilogue (warps 8-11) --
     const int q = warp & 3;
     int tl = 0, npiece = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+    for (;; ++tl) {
       const int b = tl & 1;
-      bool fin = mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) &&
-                 mbar_wait(acc_full, tl & 1, kWaitLimit) && !*abort_flag;
       // one decision for all 4 epilogue warps: they meet at named barriers below
-      fin = all_named(fin, 2, kEpiThreads);
+      bool fin = all_named(mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) && !*abort_flag, 2, kEpiThreads);
+      if (!fin) {
+        if (lane == 0) btc_flag(kStatusBtcTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      const int tile = tile_id[b];
+      if (tile < 0) break;
+      fin = all_named(mbar_wait(acc_full, tl & 1, kWaitLimit) && !*abort_flag, 2, kEpiThreads);
       if (!fin) {
         if (lane == 0) btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
@@ -507,6 +538,7 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
   a.ntx = (a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ);
   a.nty = (BC + 127) / 128;
   a.ntz = psi->ngrp;
+  a.launch_id = next_launch_id();
   CUtensorMap wide, narrow, gxm;
   int stt = encode_g(&wide, G, a, BC, 64, true);
   if (stt) return stt;

@@ -1,6 +1,7 @@
 // disco_capi.cu -- error reporting, device and argument checks of the C ABI.
 
 #include <stdarg.h>
+#include <atomic>
 #include <stdio.h>
 
 #include "disco_internal.cuh"
@@ -39,6 +40,11 @@ int check_device() {
     return fail(DISCO_ERR_UNSUPPORTED_DEVICE, "device %d is compute capability %d.%d, need 10.3", dev,
                 major, minor);
   return DISCO_OK;
+}
+
+unsigned long long next_launch_id() {
+  static std::atomic<unsigned long long> seq{0};
+  return seq.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 int check_launch(const char* what) {

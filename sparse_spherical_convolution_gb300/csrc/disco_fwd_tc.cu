@@ -37,6 +37,7 @@
 #include <cstring>
 
 #include "disco_internal.cuh"
+#include "disco_sched.cuh"
 #include "disco_umma.cuh"
 
 namespace disco {
@@ -100,6 +101,7 @@ struct TcArgs {
   int BC, Hout, Wout, Win;
   int TLB;            // table row capacity (>= every run's row length)
   int tma_store;      // X written by TMA stores (W_out % 8 == 0 and W_out >= one tile's columns)
+  unsigned long long launch_id;  // selects the scheduler slot of the persistent form
 };
 
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -454,9 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------- persistent form --
 //
-// The same tiles, items and operands, but one CTA per SM walks the tiles
-// (output row in launch order, 128 channels, NT*16 columns) round-robin and
-// its pipeline runs across tile boundaries: the next tile's x windows and
+// The same tiles, items and operands, but one CTA per SM takes tile after
+// tile (output row in launch order, 128 channels, NT*16 columns) from the
+// launch's scheduler counter (disco_sched.cuh) and hands each tile index to
+// the other roles through a 4-slot ring in shared memory.  Its pipeline runs
+// across tile boundaries: the next tile's x windows and
 // psi tables load and its T chunks build while the epilogue writes the
 // previous tile.  The epilogue has its own warps (8-11) and writes X one
 // basis function at a time ([128 channels x NT*16 columns]) through a
@@ -465,6 +469,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // epilogue to have read the previous tile out.
 constexpr int kPThreads = 384;
 constexpr int kPEpiThreads = 128;  // warps 8-11
+constexpr int kRing = 4;           // tile indices in flight between the producer and the consumers
+
+__device__ SchedSlot g_fwd_sched[kSchedSlots];
+
+// Consumer side of the tile ring: the tl-th tile index (-1 once there are no
+// more), or -2 when the wait timed out or the CTA aborts.  Every consumer
+// thread arrives on the slot's empty barrier after reading it.
+__device__ __forceinline__ int ring_take(uint64_t* full, uint64_t* empty, volatile int* ring, int tl,
+                                         volatile int* abort_flag) {
+  const int b = tl % kRing;
+  if (!mbar_wait(&full[b], (tl / kRing) & 1, kWaitLimit) || *abort_flag) return -2;
+  const int t = ring[b];
+  mbar_arrive(&empty[b]);
+  return t;
+}
 
 template <int K, int S>
 struct PCfg {
@@ -499,6 +518,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* tmem_empty = bars + 3 * STAGES + 5; // epilogue read the tile out (128 arrivals)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 7);
+  uint64_t* ring_full = bars + 3 * STAGES + 8;    // [4] tile index written (producer)
+  uint64_t* ring_empty = bars + 3 * STAGES + 12;  // [4] tile index read by every consumer
+  volatile int* ring = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 16);  // [4], -1 = no more tiles
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntx = (a.Wout + kTW * NT - 1) / (kTW * NT), nty = (a.BC + 127) / 128;
@@ -522,6 +544,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(tmem_empty, kPEpiThreads);
+    for (int b = 0; b < kRing; ++b) {
+      mbar_init(&ring_full[b], 1);
+      mbar_init(&ring_empty[b], 1 + kBuilderThreads + kPEpiThreads);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -539,7 +565,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       int i = 0, rl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      SchedSlot* slot = sched_claim(g_fwd_sched, a.launch_id, kWaitLimit);
+      if (!slot) tc_flag(kStatusTcTimeout);  // this CTA takes no tile
+      for (int tl = 0; ok; ++tl) {
+        const int rb = tl % kRing;
+        if ((tl >= kRing && !mbar_wait(&ring_empty[rb], ((tl / kRing) - 1) & 1, kWaitLimit)) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const int t = slot ? sched_next(slot) : ntiles;
+        ring[rb] = t < ntiles ? t : -1;
+        mbar_arrive(&ring_full[rb]);
+        if (t >= ntiles) break;
         int ho, bc0, wc;
         coords(t, &ho, &bc0, &wc);
         const int r_end = a.run_ptr[ho + 1];
@@ -589,6 +626,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mbar_wait(&tfull[lr & 1], (lr >> 1) & 1, kWaitLimit);
         }
       }
+      if (slot) sched_release(slot);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
@@ -596,7 +634,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(128, N);
       int i = 0, tl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+      for (; ok; ++tl) {
+        const int t = ring_take(ring_full, ring_empty, ring, tl, abort_flag);
+        if (t == -1) break;
+        if (t < 0) {
+          ok = false;
+          break;
+        }
         int ho, bc0, wc;
         coords(t, &ho, &bc0, &wc);
         if ((tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
@@ -661,7 +705,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int btid = tid - 64;
     int i = 0, rl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    for (int tl = 0; ok; ++tl) {
+      const int t = ring_take(ring_full, ring_empty, ring, tl, abort_flag);
+      ok = group_all_b(t != -2, 1, kBuilderThreads);  // one decision for the 6 warps
+      if (!ok || t == -1) break;
       int ho, bc0, wc;
       coords(t, &ho, &bc0, &wc);
       const int r_end = a.run_ptr[ho + 1];
@@ -716,8 +763,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // ---------------------------------------------- epilogue (warps 8-11) --
     const int q = warp & 3;
     const int er = q * 32 + lane;  // channel row of this thread in a piece
-    int tl = 0, npiece = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+    int npiece = 0;
+    for (int tl = 0;; ++tl) {
+      const int t = ring_take(ring_full, ring_empty, ring, tl, abort_flag);
+      if (!group_all_b(t != -2, 2, kPEpiThreads)) {
+        if (lane == 0) tc_flag(kStatusTcTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      if (t == -1) break;
       int ho, bc0, wc;
       coords(t, &ho, &bc0, &wc);
       const bool any = a.run_ptr[ho + 1] > a.run_ptr[ho];
@@ -873,6 +927,7 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
     const long long ntiles = (long long)((a.Wout + kTW * NT3 - 1) / (kTW * NT3)) * ((BC + 127) / 128) * a.Hout;
     if (ntiles > 0x7fffffffLL) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
     const int grid = (int)(ntiles < sm_count_f() ? ntiles : sm_count_f());
+    a.launch_id = next_launch_id();
     kern<<<grid, kPThreads, smem, st>>>(map, nmap, omap, a);
     return check_launch("disco_fwd (tensor cores)");
   }

@@ -19,6 +19,10 @@ int check_device();
 // Launch-error check right after a launch.
 int check_launch(const char* what);
 
+// Process-unique, nonzero id of a kernel launch (selects the launch's
+// scheduler slot, disco_sched.cuh); thread-safe.
+unsigned long long next_launch_id();
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Validates the pieces of psi every hot call relies on.

@@ -130,3 +130,40 @@ def test_workload_fwd_bwd_sampled_full_size(lib, name):
     Xs = X.view(BC, w.K, Ho, w.grid_out[1])
     got = Xs[tuple(torch.from_numpy(pts).cuda().T)].float().cpu().numpy()
     assert rel_err(got, v, S) <= TOL[w.torch_dtype]
+
+
+def test_concurrent_streams_same_psi(lib):
+    """Launches on two streams at once with one psi.  The persistent
+    tensor-core kernels hand out tiles from a counter private to each launch,
+    so every result equals the one computed alone, bit for bit."""
+    gi, go = (181, 360, 1), (181, 360, 1)
+    psi = lib.Psi(gi, go, 1, 3, 4 * math.pi / 180)
+    B, C, K = 2, 128, psi.c.K
+    g = torch.Generator(device="cuda").manual_seed(11)
+    xs = [torch.randn((B, C, gi[0], gi[1]), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3)]
+    Gs = [torch.randn((B, C, K, go[0], go[1]), generator=g, device="cuda").to(torch.bfloat16) for _ in range(3)]
+    alone_X, alone_gx = [], []
+    for x, G in zip(xs, Gs):
+        X = torch.empty((B, C, K, go[0], go[1]), dtype=torch.bfloat16, device="cuda")
+        gx = torch.empty_like(x)
+        lib.disco_fwd(psi.c, x, X, B, C)
+        lib.disco_bwd(psi.c, G, gx, B, C)
+        alone_X.append(X)
+        alone_gx.append(gx)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for rep in range(2):
+        for i, (x, G) in enumerate(zip(xs, Gs)):
+            X = torch.full((B, C, K, go[0], go[1]), float("nan"), dtype=torch.bfloat16, device="cuda")
+            gx = torch.full_like(x, float("nan"))
+            torch.cuda.synchronize()
+            sa, sb = (s1, s2) if (i + rep) % 2 == 0 else (s2, s1)
+            lib.disco_bwd(psi.c, G, gx, B, C, stream=sa)
+            lib.disco_fwd(psi.c, x, X, B, C, stream=sb)
+            lib.disco_bwd(psi.c, G, gx, B, C, stream=sb)  # same output again, racing the first
+            outs.append((i, X, gx))
+    torch.cuda.synchronize()
+    assert lib.disco_device_status(clear=True) == 0
+    for i, X, gx in outs:
+        assert torch.equal(X, alone_X[i]) and torch.equal(gx, alone_gx[i])
