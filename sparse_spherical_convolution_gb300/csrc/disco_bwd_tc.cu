@@ -40,7 +40,9 @@
 //               chunk) the psi block (bulk copy) and 1-2 G boxes (TMA);
 //   warp 1      MMA issuer (one thread);
 //   warps 2-7   build T;
-//   warps 8-11  epilogue: tcgen05.ld, bf16, 16-byte row stores.
+//   warps 8-11  epilogue: tcgen05.ld, bf16, TMA stores;
+//   warp 12     second producer: the odd items' copies (one thread issuing
+//               all 16 KB boxes caps the load rate near 35 GB/s per SM).
 // All mbarrier waits are bounded (time-out -> status flag, abort).
 
 #include <cudaTypedefs.h>
@@ -56,9 +58,10 @@ __device__ SchedSlot g_btc_sched[kSchedSlots];
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;
 constexpr int kBuilderThreads = 192;        // warps 2-7
 constexpr int kEpiThreads = 128;            // warps 8-11
+constexpr int kProducers = 2;               // warps 0 and 12 issue the even / odd items' copies
 constexpr int kN = 256;                     // MMA N = 8 rows x 32 columns
 constexpr int kNT = 2;                      // column blocks per tile
 constexpr int kStages = 3;
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&info_full[b], 1);
-      mbar_init(&info_empty[b], 1 + kBuilderThreads + kEpiThreads);
+      mbar_init(&info_empty[b], kProducers - 1 + 1 + kBuilderThreads + kEpiThreads);
     }
     mbar_init(acc_full, 1);
     mbar_init(tmem_empty, kEpiThreads);
@@ -201,10 +204,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
+  // Copies of item i (stage i % kStages): the psi block and the 1-2 G boxes.
+  // Issued by producer i & 1 after the stage's previous MMAs completed.
+  auto issue_item = [&](int i, const disco_grp_ent& en, int k, int c, int qb, int bc0) -> bool {
+    const int s = i % kStages;
+    if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag)
+      return false;
+    uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
+    const int nsteps = min(4, (int)en.KB - 4 * c);
+    const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
+    mbar_expect_tx(&fullA[s], nbox * kBoxBytes + Cfg::kTabBytes);
+    bulk_copy(st + 2 * kBoxBytes + kTBytes, a.gtab + en.off + (size_t)(k * en.nch + c) * grp_block(S),
+              Cfg::kTabBytes, &fullA[s]);
+    const int row = k * a.Hout + en.ho;
+    for (int bb = 0; bb < nbox; ++bb) {
+      const int col0 = qb - en.MW + 64 * (c + bb);
+      uint8_t* dst = st + bb * kBoxBytes;
+      if (!box_is_narrow(col0, a.Wout)) {
+        tma_load_3d(dst, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
+      } else {
+        for (int g = 0; g < 8; ++g)
+          tma_load_3d(dst + g * kNarrowBytes, &gnarrow, wrapc(col0 + 8 * g, a.Wout), row, bc0, &fullA[s]);
+      }
+    }
+    return true;
+  };
+  // after a failure: let this producer's copies in flight land before the CTA
+  // exits (n = one past its last issued item)
+  auto drain_own = [&](int n, int who) {
+    for (int li = n - 1; li >= 0 && li >= n - 2 * kStages; --li)
+      if ((li & 1) == who) mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
+  };
+
   if (warp == 0) {
-    // ---------------------------------------------------------- producer --
+    // ------------------------------------------- producer (even items) --
     if (lane == 0) {
-      int i = 0, tl = 0;
+      int i = 0, tl = 0, done = 0;  // done: one past the last item this thread issued
       bool ok = true;
       SchedSlot* slot = sched_claim(g_btc_sched, a.launch_id, kWaitLimit);
       if (!slot) btc_flag(kStatusBtcTimeout);  // this CTA takes no tile
@@ -241,43 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < ne && ok; ++j) {
           const disco_grp_ent en = info[j];
           for (int k = 0; k < a.K && ok; ++k)
-            for (int c = 0; c < en.nch; ++c, ++i) {
-              const int s = i % kStages;
-              if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) ||
-                  *abort_flag) {
-                ok = false;
-                break;
-              }
-              uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
-              const int nsteps = min(4, (int)en.KB - 4 * c);
-              const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
-              mbar_expect_tx(&fullA[s], nbox * kBoxBytes + Cfg::kTabBytes);
-              bulk_copy(st + 2 * kBoxBytes + kTBytes,
-                        a.gtab + en.off + (size_t)(k * en.nch + c) * grp_block(S), Cfg::kTabBytes,
-                        &fullA[s]);
-              const int row = k * a.Hout + en.ho;
-              for (int bb = 0; bb < nbox; ++bb) {
-                const int col0 = qb - en.MW + 64 * (c + bb);
-                uint8_t* slot = st + bb * kBoxBytes;
-                if (!box_is_narrow(col0, a.Wout)) {
-                  tma_load_3d(slot, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
-                } else {
-                  for (int g = 0; g < 8; ++g)
-                    tma_load_3d(slot + g * kNarrowBytes, &gnarrow, wrapc(col0 + 8 * g, a.Wout), row, bc0,
-                                &fullA[s]);
-                }
-              }
-            }
+            for (int c = 0; c < en.nch && ok; ++c, ++i)
+              if ((i & 1) == 0 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
         }
       }
       if (!ok) {
         btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
-        // let the copies in flight land before the CTA exits
-        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
-          const int li = i - back;
-          mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
-        }
+        drain_own(done, 0);
       }
       if (slot) sched_release(slot);
     }
@@ -399,6 +405,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       btc_flag(kStatusBtcTimeout);
       *abort_flag = 1;
     }
+  } else if (warp == 12) {
+    // -------------------------------------------- producer (odd items) --
+    if (lane == 0) {
+      int i = 0, done = 0;
+      bool ok = true;
+      for (int tl = 0; ok; ++tl) {
+        const int b = tl & 1;
+        if (!mbar_wait(&info_full[b], (tl >> 1) & 1, kWaitLimit) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const int tile = tile_id[b];
+        if (tile < 0) break;
+        int qb, bc0, zg;
+        tile_coords<S>(a, tile, &qb, &bc0, &zg);
+        const int ne = info_cnt[b];
+        const disco_grp_ent* info = infos + b * kMaxEnt;
+        for (int j = 0; j < ne && ok; ++j) {
+          const disco_grp_ent en = info[j];
+          for (int k = 0; k < a.K && ok; ++k)
+            for (int c = 0; c < en.nch && ok; ++c, ++i)
+              if ((i & 1) == 1 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
+        }
+        if (!ok) break;
+        mbar_arrive(&info_empty[b]);
+      }
+      if (!ok) {
+        btc_flag(kStatusBtcTimeout);
+        *abort_flag = 1;
+        drain_own(done, 1);
+      }
+    }
   } else {
     // ----------------------------------------------- epilogue (warps 8-11) --
     const int q = warp & 3;
@@ -506,11 +544,19 @@ int sm_count() {
   return n;
 }
 
-int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw, bool swz) {
+// G as [column][row k*H_out + ho][channel]: in the API layout [BC][K*H_out][W_out]
+// (channel rows a K*H_out*W_out slab apart) or, for an intermediate the
+// library writes itself, [K*H_out][BC][W_out] (channel rows W_out apart, which
+// lets a 128-channel box stream far faster).  Same boxes and coordinates.
+int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw, bool swz, bool rows_of_channels) {
   auto enc = encode_fn_b();
   if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {(cuuint64_t)a.Wout, (cuuint64_t)a.K * a.Hout, (cuuint64_t)BC};
   cuuint64_t strides[2] = {(cuuint64_t)a.Wout * 2, (cuuint64_t)a.K * a.Hout * a.Wout * 2};
+  if (rows_of_channels) {
+    strides[0] = (cuuint64_t)BC * a.Wout * 2;
+    strides[1] = (cuuint64_t)a.Wout * 2;
+  }
   cuuint32_t box[3] = {(cuuint32_t)boxw, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(G), dims, strides, box, estr,
@@ -522,7 +568,7 @@ int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw
 }
 
 template <int S>
-int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st) {
+int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool roc) {
   using Cfg = BCfg<S>;
   BtcArgs a;
   a.gx = (__nv_bfloat16*)gx;
@@ -540,9 +586,9 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
   a.ntz = psi->ngrp;
   a.launch_id = next_launch_id();
   CUtensorMap wide, narrow, gxm;
-  int stt = encode_g(&wide, G, a, BC, 64, true);
+  int stt = encode_g(&wide, G, a, BC, 64, true, roc);
   if (stt) return stt;
-  if ((stt = encode_g(&narrow, G, a, BC, 8, false))) return stt;
+  if ((stt = encode_g(&narrow, G, a, BC, 8, false, roc))) return stt;
   {
     // gx as the TMA store target: [B*C][H_in][W_in], box 32 columns x 1 row x 128 channels
     cuuint64_t dims[3] = {(cuuint64_t)a.Win, (cuuint64_t)a.Hin, (cuuint64_t)BC};
@@ -576,15 +622,19 @@ cudaError_t btc_status(int32_t* v, bool clear) {
   return e;
 }
 
-int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st) {
+bool bwd_tc_supported(const disco_psi* psi, int BC) {
   const int Win = psi->grid_in.nlon, Wout = psi->grid_out.nlon, Hin = psi->grid_in.nlat;
-  if ((psi->s != 1 && psi->s != 2) || Wout % 8 != 0 || Win % 8 != 0 || Wout < 64 || BC < 1 ||
-      psi->K > 16 || !psi->grp_ptr || !psi->grp || !psi->gtab || psi->ngrp_ent < 1 ||
-      psi->ngrp != (Hin + kGrpRows - 1) / kGrpRows || psi->grp_max > kMaxEnt ||
-      (long long)psi->K * psi->grid_out.nlat > (1 << 30))
-    return DISCO_ERR_UNSUPPORTED;
+  return (psi->s == 1 || psi->s == 2) && Wout % 8 == 0 && Win % 8 == 0 && Wout >= 64 && BC >= 1 &&
+         psi->K <= 16 && psi->grp_ptr && psi->grp && psi->gtab && psi->ngrp_ent >= 1 &&
+         psi->ngrp == (Hin + kGrpRows - 1) / kGrpRows && psi->grp_max <= kMaxEnt &&
+         (long long)psi->K * psi->grid_out.nlat <= (1 << 30);
+}
+
+int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool rows_of_channels) {
+  if (!bwd_tc_supported(psi, BC)) return DISCO_ERR_UNSUPPORTED;
   static_assert(BCfg<1>::kSmem <= 227 * 1024 && BCfg<2>::kSmem <= 227 * 1024, "shared memory");
-  return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st) : launch_btc<2>(psi, G, gx, BC, st);
+  return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st, rows_of_channels)
+                     : launch_btc<2>(psi, G, gx, BC, st, rows_of_channels);
 }
 
 }  // namespace disco

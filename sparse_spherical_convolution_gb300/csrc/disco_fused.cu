@@ -705,6 +705,15 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   g.CK = Cin * psi->K;
   g.P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   cudaStream_t s = (cudaStream_t)stream;
+  if (dx_tensor_core_supported(Cout, g.CK, g.P) && bwd_tc_supported(psi, B * Cin)) {
+    // both on the tensor cores: dX goes through the workspace as
+    // [K*H_out][B*Cin][W_out], whose 128-channel boxes the transpose streams
+    // much faster than boxes of the [B*Cin][K][H_out][W_out] layout
+    const int roc[4] = {psi->K, psi->grid_out.nlat, psi->grid_out.nlon, Cin};
+    st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s, roc);
+    if (st) return st;
+    return bwd_tensor_core(psi, workspace, gx, B * Cin, s, true);
+  }
   st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s);
   if (st == DISCO_ERR_UNSUPPORTED) {
     if (cudaFuncSetAttribute(dx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -89,7 +89,12 @@ __host__ __device__ constexpr uint32_t idesc_mn(int M, int N, bool b_mn) {
 }
 
 struct GemmTcArgs {
-  __nv_bfloat16* out;  // [B][Nt][P]
+  __nv_bfloat16* out;  // [B][Nt][P], or the row-of-channels form below when ctK > 0
+  // Row-of-channels output (dX of the input gradient, n = c*K + k, p = ho*W + wo):
+  //   out[(k*ctH + ho)][b*ctC + c][wo]
+  // so that a TMA box of 128 channels x 64 columns of one row (k, ho) reads
+  // rows W*2 bytes apart instead of a channel slab apart.
+  int ctK, ctH, ctW, ctC;
   uint32_t bbytes;     // bytes of the B boxes of one stage
   int64_t P;           // pixels
   int Kt;              // reduction length j
@@ -246,6 +251,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t pw = p0 + q * 32;  // this warp's first pixel
       uint16_t* stg = epi_stage + (warp - 2) * (kEpiStage / 2);
       __nv_bfloat16* ob = a.out + (size_t)b * a.Nt * a.P;
+      // row-of-channels form: this lane's pixel segment (row ho, column wo) is
+      // fixed for the tile; its two outputs per step, n = n0 + c0 + lane/4 + 8h,
+      // advance by 16 per step, so (c, k) = divmod(n, K) is carried along
+      const int64_t BC = (int64_t)a.B * a.ctC;
+      int64_t rho = 0, rwo = 0;
+      int rc[2] = {0, 0}, rk[2] = {0, 0}, dc = 0, dk = 0;
+      if (a.ctK > 0) {
+        const int64_t pp = pw + (lane & 3) * 8;
+        rho = pp / a.ctW;
+        rwo = pp - rho * a.ctW;
+        dc = 16 / a.ctK;
+        dk = 16 - dc * a.ctK;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = n0 + (lane >> 2) + 8 * h;
+          rc[h] = n / a.ctK;
+          rk[h] = n - rc[h] * a.ctK;
+        }
+      }
       for (int c0 = 0; c0 < a.NB; c0 += 16) {
         float v[16];
         tmem_ld16(tmem + ab * 256 + ((uint32_t)(q * 32) << 16) + c0, v);
@@ -257,11 +281,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int idx = lane + 32 * h, row = idx >> 2, seg = idx & 3;
           const int n = n0 + c0 + row;
           const int64_t pp = pw + seg * 8;  // P % 8 == 0: a segment is all in or all out
-          if (n < a.Nt && pp < a.P)
-            *reinterpret_cast<uint4*>(ob + (size_t)n * a.P + pp) =
-                *reinterpret_cast<const uint4*>(stg + row * 32 + seg * 8);
+          if (n < a.Nt && pp < a.P) {
+            __nv_bfloat16* dst;
+            if (a.ctK > 0)  // W % 8 == 0: the 8 pixels lie in one row
+              dst = a.out + (((int64_t)rk[h] * a.ctH + rho) * BC + (int64_t)b * a.ctC + rc[h]) * a.ctW + rwo;
+            else
+              dst = ob + (size_t)n * a.P + pp;
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(stg + row * 32 + seg * 8);
+          }
         }
         __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // next step: n += 16
+          rc[h] += dc;
+          rk[h] += dk;
+          if (rk[h] >= a.ctK) {
+            rk[h] -= a.ctK;
+            ++rc[h];
+          }
+        }
       }
       tc_fence_before();
       mbar_arrive(&acce[ab]);
@@ -505,9 +543,14 @@ int sm_count_g() {
 
 // out[b][n][p] = sum_j A[b][j][p] * Bop(j, n); W is [Nt][Kt] (kBMN false) or [Kt][Nt] (true)
 template <bool kBMN>
-int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, int64_t P, cudaStream_t st) {
+int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, int64_t P, cudaStream_t st,
+                const int* ct = nullptr) {
   GemmTcArgs g;
   g.out = (__nv_bfloat16*)out;
+  g.ctK = ct ? ct[0] : 0;
+  g.ctH = ct ? ct[1] : 0;
+  g.ctW = ct ? ct[2] : 0;
+  g.ctC = ct ? ct[3] : 0;
   g.P = P;
   g.Kt = Kt;
   g.Nt = Nt;
@@ -553,9 +596,16 @@ int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int
   return launch_gemm<false>(X, W, y, B, CK, Cout, P, st);
 }
 
-int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P, cudaStream_t st) {
-  if (!gemm_tc_supported(P, Cout, CK) || CK % 64 != 0) return DISCO_ERR_UNSUPPORTED;
-  return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st);
+bool dx_tensor_core_supported(int Cout, int CK, int64_t P) { return gemm_tc_supported(P, Cout, CK) && CK % 64 == 0; }
+
+int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P, cudaStream_t st,
+                   const int* rows_of_channels) {
+  if (!dx_tensor_core_supported(Cout, CK, P)) return DISCO_ERR_UNSUPPORTED;
+  if (rows_of_channels) {
+    const int K = rows_of_channels[0], H = rows_of_channels[1], W_ = rows_of_channels[2], C = rows_of_channels[3];
+    if (K < 1 || C < 1 || W_ % 8 != 0 || (int64_t)K * C != CK || (int64_t)H * W_ != P) return DISCO_ERR_UNSUPPORTED;
+  }
+  return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st, rows_of_channels);
 }
 
 namespace {

@@ -38,7 +38,10 @@ cudaError_t tc_status(int32_t* v, bool clear);
 
 // Transpose contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
 // without launching, for shapes that path does not take.
-int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st);
+// rows_of_channels: G is [K*H_out][BC][W_out] instead of [BC][K*H_out][W_out].
+int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st,
+                    bool rows_of_channels = false);
+bool bwd_tc_supported(const disco_psi* psi, int BC);
 cudaError_t btc_status(int32_t* v, bool clear);
 
 // Dense GEMMs of the fused paths on the tensor cores (TMA-fed tcgen05):
@@ -47,8 +50,11 @@ cudaError_t btc_status(int32_t* v, bool clear);
 // DISCO_ERR_UNSUPPORTED, without launching, for shapes they do not take.
 int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P,
                        cudaStream_t st);
+// rows_of_channels = {K, H_out, W_out, C} (or null): write dX as
+// [K*H_out][B*C][W_out] instead of [B][C*K][P] (W_out % 8 == 0).
+bool dx_tensor_core_supported(int Cout, int CK, int64_t P);
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P,
-                   cudaStream_t st);
+                   cudaStream_t st, const int* rows_of_channels = nullptr);
 cudaError_t gemm_status(int32_t* v, bool clear);
 // Weight gradient dW[o][j] = sum_b sum_p dy[b][o][p] X[b][j][p] (split reduction
 // through fp32 partials of dw_partial_bytes bytes, then rounded to bf16).
