@@ -53,6 +53,8 @@ def _load():
         lib.oracle_colat.argtypes = [i32, i32, i32]
         lib.oracle_quad.restype = f64
         lib.oracle_quad.argtypes = [i32, i32, i32]
+        lib.oracle_gauss_node.restype = None
+        lib.oracle_gauss_node.argtypes = [i32, i32, P, P]
         lib.oracle_hat.restype = f64
         lib.oracle_hat.argtypes = [f64, i32, f64]
         lib.oracle_geometry.restype = None
@@ -116,6 +118,13 @@ def colat(nlat: int, poles: int, i: int) -> float:
 
 def quad(nlat: int, poles: int, i: int) -> float:
     return _load().oracle_quad(nlat, poles, i)
+
+
+def gauss_node(n: int, i: int):
+    """(x_i, w_i): the i-th Gauss-Legendre node of order n (descending) and its weight."""
+    x, w = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_gauss_node(n, i, ctypes.byref(x), ctypes.byref(w))
+    return x.value, w.value
 
 
 def hat(d: float, r: int, width: float) -> float:

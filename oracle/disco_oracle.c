@@ -17,6 +17,10 @@
  *
  *   grids      midpoint:  theta_i = (i + 1/2) pi / H
  *              poles:     theta_i = i pi / (H - 1)   (theta_{H-1} = pi exactly)
+ *              Legendre-Gauss: theta_i = arccos x_i, x_0 > x_1 > ... the H
+ *                         roots of the Legendre polynomial P_H (north to
+ *                         south), found by Newton's method on the three-term
+ *                         recurrence
  *              longitude: phi_j   = 2 pi j / W
  *   distance   haversine great-circle distance between the output point
  *              (theta_o, phi = 0) and the input point (theta_i, dphi),
@@ -31,7 +35,10 @@
  *                                           A_2 = sin beta (0 when d < 1e-12)
  *              indicator:   K = 1, psi = 1 on d < cutoff (no quadrature, no
  *                           normalisation; closed-form test basis only)
- *   quadrature q_i = sin theta_i, exactly 0 on the pole rows of a pole grid
+ *   quadrature q_i = sin theta_i, exactly 0 on the pole rows of a pole grid;
+ *              Legendre-Gauss: the Gauss-Legendre weight
+ *              w_i = 2 / ((1 - x_i^2) P_H'(x_i)^2), which carries the sin
+ *              theta d theta of the area element
  *   support    entry (r, hi, wi) is structural iff h_r(d) > 1e-9 and q_i > 0
  *   normaliser N(r, ho) = sum over the structural entries of ring r of h_r q_i
  *   value      psi[k, ho, hi, wi] = h_r(d) A_a(beta) q_i / N(r, ho)
@@ -69,7 +76,74 @@ typedef struct {
 
 /* ---------------------------------------------------------------- grids -- */
 
+/* Gauss-Legendre node x_i (descending in i) and weight of order n: Newton's
+   method from the standard first guess cos(pi (i + 3/4) / (n + 1/2)), with
+   P_n and P_n' from the three-term recurrence. */
+void oracle_gauss_node(int32_t n, int32_t i, double* x_out, double* w_out) {
+  double x = cos(OR_PI * ((double)i + 0.75) / ((double)n + 0.5));
+  double dp = 1.0;
+  for (int it = 0; it < 100; ++it) {
+    double p0 = 1.0, p1 = x;
+    for (int32_t j = 1; j < n; ++j) {
+      double p2 = ((2.0 * j + 1.0) * x * p1 - (double)j * p0) / ((double)j + 1.0);
+      p0 = p1;
+      p1 = p2;
+    }
+    dp = (double)n * (x * p1 - p0) / -((1.0 - x) * (1.0 + x)); /* P_n'(x), p0 = P_{n-1} */
+    double dx = p1 / dp;
+    x -= dx;
+    if (fabs(dx) <= 1e-15) break; /* quadratic convergence: x is now within an ulp or two */
+  }
+  { /* derivative at the converged node */
+    double p0 = 1.0, p1 = x;
+    for (int32_t j = 1; j < n; ++j) {
+      double p2 = ((2.0 * j + 1.0) * x * p1 - (double)j * p0) / ((double)j + 1.0);
+      p0 = p1;
+      p1 = p2;
+    }
+    dp = (double)n * (x * p1 - p0) / -((1.0 - x) * (1.0 + x));
+  }
+  *x_out = x;
+  *w_out = 2.0 / ((1.0 - x) * (1.0 + x) * dp * dp);
+}
+
+/* Gauss-Legendre colatitudes and weights of one order, computed once and kept
+   (a few orders at a time; the oracle calls these per row in its loops). */
+typedef struct { int32_t n; double* th; double* w; } or_gauss;
+static or_gauss or_gauss_cache[8];
+static const or_gauss* or_gauss_table(int32_t n) {
+  const or_gauss* r = NULL;
+#pragma omp critical(or_gauss_lock)
+  {
+    for (int c = 0; c < 8 && !r; ++c)
+      if (or_gauss_cache[c].n == n && or_gauss_cache[c].th) r = &or_gauss_cache[c];
+    if (!r) {
+      int slot = 0;
+      while (slot < 8 && or_gauss_cache[slot].th) ++slot;
+      if (slot == 8) { /* full: reuse slot 0 */
+        free(or_gauss_cache[0].th);
+        free(or_gauss_cache[0].w);
+        or_gauss_cache[0].th = NULL;
+        slot = 0;
+      }
+      double* th = (double*)malloc(sizeof(double) * (size_t)n);
+      double* w = (double*)malloc(sizeof(double) * (size_t)n);
+      for (int32_t i = 0; i < n; ++i) {
+        double x;
+        oracle_gauss_node(n, i, &x, &w[i]);
+        th[i] = acos(x);
+      }
+      or_gauss_cache[slot].n = n;
+      or_gauss_cache[slot].w = w;
+      or_gauss_cache[slot].th = th;
+      r = &or_gauss_cache[slot];
+    }
+  }
+  return r;
+}
+
 double oracle_colat(int32_t nlat, int32_t poles, int32_t i) {
+  if (poles == 2) return or_gauss_table(nlat)->th[i];
   if (poles) {
     if (i == nlat - 1) return OR_PI;
     return (double)i * OR_PI / (double)(nlat - 1);
@@ -78,6 +152,7 @@ double oracle_colat(int32_t nlat, int32_t poles, int32_t i) {
 }
 
 double oracle_quad(int32_t nlat, int32_t poles, int32_t i) {
+  if (poles == 2) return or_gauss_table(nlat)->w[i];
   if (poles && (i == 0 || i == nlat - 1)) return 0.0;
   return sin(oracle_colat(nlat, poles, i));
 }

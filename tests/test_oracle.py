@@ -31,10 +31,16 @@ TINY = [
     ((17, 32, 1), (9, 16, 1), oracle.ANISO, 2, 3 * math.pi / 8),
     ((12, 24, 0), (12, 24, 0), oracle.ANISO, 3, 4 * math.pi / 12),
     ((8, 16, 0), (8, 8, 0), oracle.ISO, 2, 3 * math.pi / 8),   # s = 2 with equal rows
+    ((8, 16, 2), (8, 16, 2), oracle.ISO, 3, 2 * math.pi / 8),   # Legendre-Gauss grids
+    ((16, 32, 0), (8, 16, 2), oracle.ANISO, 3, 3 * math.pi / 8),  # equiangular -> Legendre-Gauss, s = 2
 ]
 
 
 def _colats(nlat, poles):
+    if poles == 2:
+        # numpy's Gauss-Legendre rule (ascending nodes): colatitudes north to south
+        x, w = np.polynomial.legendre.leggauss(nlat)
+        return np.arccos(x[::-1]), w[::-1].copy()
     if poles:
         th = np.arange(nlat) * math.pi / (nlat - 1)
         th[-1] = math.pi
@@ -190,6 +196,29 @@ def test_closed_form_golden_2x4():
             assert abs(psi.val[e, k] - v) < 1e-15, (kn, k, hi, wi)
 
 
+@pytest.mark.parametrize("n", [2, 3, 16, 64, 361])
+def test_gauss_legendre_nodes_and_weights(n):
+    """Legendre-Gauss grid: nodes and weights against numpy's Gauss-Legendre
+    rule, the weight sum 2, exactness on polynomials of degree < 2n, and the
+    grid's colatitudes (ascending, symmetric about the equator)."""
+    xs, ws = np.polynomial.legendre.leggauss(n)
+    got = np.array([oracle.gauss_node(n, i) for i in range(n)])
+    assert np.all(np.diff(got[:, 0]) < 0)
+    assert np.abs(got[::-1, 0] - xs).max() < 1e-14
+    # absolute: numpy's own weights are off by a few 1e-15 for large n (the
+    # exactness checks below pin ours more tightly)
+    assert np.abs(got[::-1, 1] - ws).max() < 2e-14
+    assert abs(got[:, 1].sum() - 2.0) < 1e-13
+    for deg in (0, 1, 2, 2 * n - 2, 2 * n - 1):
+        exact = 0.0 if deg % 2 else 2.0 / (deg + 1)
+        assert abs(np.sum(got[:, 1] * got[:, 0] ** deg) - exact) < 1e-12
+    th = np.array([oracle.colat(n, 2, i) for i in range(n)])
+    q = np.array([oracle.quad(n, 2, i) for i in range(n)])
+    assert np.all(np.diff(th) > 0) and th[0] > 0 and th[-1] < math.pi
+    assert np.abs(th + th[::-1] - math.pi).max() < 1e-13
+    assert np.array_equal(q, got[:, 1])
+
+
 def test_hat_partition_of_unity_and_nodes():
     width = 0.1
     for R in (2, 3, 5):
@@ -230,7 +259,7 @@ def test_constant_field_and_symmetries(case):
             # 1 wherever ring r has support; a ring with no support (only
             # possible next to a zero-weight pole row) gives exactly 0
             assert ((np.abs(rows - 1) < 1e-13) | (rows == 0)).all()
-            if not go[2]:
+            if go[2] != 1:
                 assert np.abs(rows - 1).max() < 1e-13
         elif a == 2:
             assert np.abs(rows).max() < 1e-13
