@@ -54,9 +54,14 @@ typedef enum {
 
 typedef enum { DISCO_F32 = 0, DISCO_BF16 = 1 } disco_dtype;
 
-/* Equiangular grid.  poles = 0: colatitude (i + 1/2) pi / nlat;
-   poles = 1: colatitude i pi / (nlat - 1) (both poles on the grid).
-   Longitude 2 pi j / nlon in both cases. */
+/* Latitude rows of a grid.  poles = 0 (equiangular, midpoints): colatitude
+   (i + 1/2) pi / nlat; poles = 1 (equiangular, both poles on the grid):
+   colatitude i pi / (nlat - 1); poles = 2 (Legendre-Gauss, the grid the
+   DISCO Kernel Development Guide's benchmark shapes name "legendre-gauss"):
+   colatitude arccos x_i with x_0 > x_1 > ... the roots of the Legendre
+   polynomial P_nlat, and the Gauss-Legendre weight of row i as the input
+   quadrature weight (sin(colatitude) on the equiangular grids).
+   Longitude 2 pi j / nlon on every grid. */
 typedef struct {
   int32_t nlat, nlon, poles;
 } disco_grid;

@@ -46,9 +46,10 @@ constexpr double kCoincident = 1e-12;
 constexpr int kMaxRad = 8;
 
 struct PsiGeom {
-  int Hin, Win, pin, Hout, Wout, pout;
+  int Hin, Win, pin, Hout, Wout, pout;  // pin / pout: 0 midpoint, 1 poles, 2 Legendre-Gauss
   int kind, R, K, Kp;
   double cutoff, width;
+  const double* lg;  // workspace table [theta_in (Hin) | w_in (Hin) | theta_out (Hout)] for Legendre-Gauss grids
 };
 
 __device__ double colat(int H, int poles, int i) {
@@ -62,6 +63,44 @@ __device__ double colat(int H, int poles, int i) {
 __device__ double quadw(int H, int poles, int i) {
   if (poles && (i == 0 || i == H - 1)) return 0.0;
   return sin(colat(H, poles, i));
+}
+
+// Legendre-Gauss node i of order n (descending x): Newton's method on P_n
+// from cos(pi (i + 3/4) / (n + 1/2)), P_n and P_n' by the three-term
+// recurrence; the weight 2 / ((1 - x^2) P_n'(x)^2).
+__device__ void gauss_node(int n, int i, double* x_out, double* w_out) {
+  double x = cos(kPi * ((double)i + 0.75) / ((double)n + 0.5));
+  double pn = 0.0, pm = 0.0;
+  for (int it = 0; it < 100; ++it) {
+    pm = 1.0;
+    pn = x;
+    for (int j = 1; j < n; ++j) {
+      const double nx = ((2.0 * j + 1.0) * x * pn - (double)j * pm) / ((double)j + 1.0);
+      pm = pn;
+      pn = nx;
+    }
+    const double dp = (double)n * (x * pn - pm) / -((1.0 - x) * (1.0 + x));
+    const double dx = pn / dp;
+    x -= dx;
+    if (fabs(dx) <= 1e-15) break;
+  }
+  pm = 1.0;
+  pn = x;
+  for (int j = 1; j < n; ++j) {
+    const double nx = ((2.0 * j + 1.0) * x * pn - (double)j * pm) / ((double)j + 1.0);
+    pm = pn;
+    pn = nx;
+  }
+  const double dp = (double)n * (x * pn - pm) / -((1.0 - x) * (1.0 + x));
+  *x_out = x;
+  *w_out = 2.0 / ((1.0 - x) * (1.0 + x) * dp * dp);
+}
+
+// Colatitude and quadrature weight of a row of the input / output grid.
+__device__ double th_in(const PsiGeom& g, int i) { return g.pin == 2 ? g.lg[i] : colat(g.Hin, g.pin, i); }
+__device__ double q_in(const PsiGeom& g, int i) { return g.pin == 2 ? g.lg[g.Hin + i] : quadw(g.Hin, g.pin, i); }
+__device__ double th_out(const PsiGeom& g, int i) {
+  return g.pout == 2 ? g.lg[2 * g.Hin + i] : colat(g.Hout, g.pout, i);
 }
 
 // distance and bearing from (th_o, 0) to (th_i, 2 pi delta / W)
@@ -148,6 +187,7 @@ struct Workspace {
   int32_t* tcount;    // [Hin + 1]
   int32_t* gcnt;      // [ngroups][2]: entries, blocks of each input-row group
   int32_t* gboff;     // [ngroups]: first block of each group
+  double* lg;         // [2 Hin + Hout]: Legendre-Gauss colatitudes and input weights
 };
 
 __host__ __device__ inline int num_groups(const PsiGeom& g) { return (g.Hin + kGrpRows - 1) / kGrpRows; }
@@ -175,20 +215,37 @@ size_t carve_workspace(const PsiGeom& g, char* base, Workspace* ws) {
   w.tcount = (int32_t*)take((size_t)(g.Hin + 1) * 4);
   w.gcnt = (int32_t*)take((size_t)num_groups(g) * 2 * 4);
   w.gboff = (int32_t*)take((size_t)num_groups(g) * 4);
+  w.lg = (double*)take((size_t)(2 * g.Hin + g.Hout) * 8);
   if (ws) *ws = w;
   return o;
 }
 
 // ------------------------------------------------------------- kernels --
 
+// Legendre-Gauss tables of the grids that use them; one thread per row.
+__global__ void lg_kernel(PsiGeom g, Workspace ws) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  double x, w;
+  if (t < g.Hin) {
+    if (g.pin != 2) return;
+    gauss_node(g.Hin, t, &x, &w);
+    ws.lg[t] = acos(x);
+    ws.lg[g.Hin + t] = w;
+  } else if (t < g.Hin + g.Hout) {
+    if (g.pout != 2) return;
+    gauss_node(g.Hout, t - g.Hin, &x, &w);
+    ws.lg[2 * g.Hin + (t - g.Hin)] = acos(x);
+  }
+}
+
 // One block per output row; threads stride over input rows.
 __global__ void count_kernel(PsiGeom g, Workspace ws) {
   int ho = blockIdx.x;
-  double th_o = colat(g.Hout, g.pout, ho);
+  double th_o = th_out(g, ho);
   for (int hi = threadIdx.x; hi < g.Hin; hi += blockDim.x) {
     size_t t = (size_t)ho * g.Hin + hi;
-    double th_i = colat(g.Hin, g.pin, hi);
-    double q = quadw(g.Hin, g.pin, hi);
+    double th_i = th_in(g, hi);
+    double q = q_in(g, hi);
     int cnt[kMaxRad] = {0};
     double hqs[kMaxRad] = {0};
     int m = -1;
@@ -315,15 +372,15 @@ __global__ void offsets_kernel(PsiGeom g, Workspace ws, PsiOut p) {
 // writes one whole run in neighbour order.
 __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   int ho = blockIdx.x;
-  double th_o = colat(g.Hout, g.pout, ho);
+  double th_o = th_out(g, ho);
   double nrm[kMaxRad];
   for (int r = 0; r < g.R; ++r) nrm[r] = ws.norm[(size_t)ho * g.R + r];
   for (int hi = threadIdx.x; hi < g.Hin; hi += blockDim.x) {
     size_t t = (size_t)ho * g.Hin + hi;
     int m = ws.mtab[t];
     if (m < 0) continue;
-    double th_i = colat(g.Hin, g.pin, hi);
-    double q = quadw(g.Hin, g.pin, hi);
+    double th_i = th_in(g, hi);
+    double q = q_in(g, hi);
     int W = g.Win, hr = half_ring(W);
     int len = run_len(m, W);
     bool full = (len == W);
@@ -562,7 +619,9 @@ int make_geom(const disco_grid* gi, const disco_grid* go, const disco_basis* b, 
   if (!gi || !go || !b) return fail(DISCO_ERR_INVALID_ARG, "null grid or basis");
   if (gi->nlat < 2 || go->nlat < 2 || gi->nlon < 1 || go->nlon < 1)
     return fail(DISCO_ERR_INVALID_ARG, "grid too small (nlat >= 2, nlon >= 1)");
-  if ((gi->poles && gi->nlat < 3) || (go->poles && go->nlat < 3))
+  if (gi->poles < 0 || gi->poles > 2 || go->poles < 0 || go->poles > 2)
+    return fail(DISCO_ERR_INVALID_ARG, "grid poles must be 0 (midpoint), 1 (poles) or 2 (Legendre-Gauss)");
+  if ((gi->poles == 1 && gi->nlat < 3) || (go->poles == 1 && go->nlat < 3))
     return fail(DISCO_ERR_INVALID_ARG, "pole grid needs nlat >= 3");
   if (gi->nlon % go->nlon != 0)
     return fail(DISCO_ERR_UNSUPPORTED, "W_in (%d) must be a multiple of W_out (%d)", gi->nlon, go->nlon);
@@ -577,16 +636,17 @@ int make_geom(const disco_grid* gi, const disco_grid* go, const disco_basis* b, 
     return fail(DISCO_ERR_UNSUPPORTED, "input grid too large for int32 indices");
   g->Hin = gi->nlat;
   g->Win = gi->nlon;
-  g->pin = gi->poles ? 1 : 0;
+  g->pin = gi->poles;
   g->Hout = go->nlat;
   g->Wout = go->nlon;
-  g->pout = go->poles ? 1 : 0;
+  g->pout = go->poles;
   g->kind = b->kind;
   g->R = b->n_radial;
   g->K = K;
   g->Kp = (K + 7) / 8 * 8;
   g->cutoff = b->cutoff;
   g->width = b->cutoff / (double)b->n_radial;
+  g->lg = nullptr;
   return DISCO_OK;
 }
 
@@ -650,7 +710,12 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
     return fail(DISCO_ERR_ALIGNMENT, "psi workspace must be 256-byte aligned");
   Workspace ws;
   carve_workspace(g, (char*)workspace, &ws);
+  g.lg = ws.lg;
   cudaStream_t s = (cudaStream_t)stream;
+  if (g.pin == 2 || g.pout == 2) {
+    lg_kernel<<<(g.Hin + g.Hout + 127) / 128, 128, 0, s>>>(g, ws);
+    if ((st = check_launch("psi Legendre-Gauss nodes"))) return st;
+  }
   count_kernel<<<g.Hout, 128, 0, s>>>(g, ws);
   if ((st = check_launch("psi count"))) return st;
   rowsum_kernel<<<(g.Hout + 127) / 128, 128, 0, s>>>(g, ws);
@@ -730,6 +795,7 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
     return fail(DISCO_ERR_WORKSPACE, "psi workspace needs %zu bytes", need);
   Workspace ws;
   carve_workspace(g, (char*)workspace, &ws);
+  g.lg = ws.lg;  // Legendre-Gauss tables left in the workspace by disco_psi_plan
   PsiOut p;
   carve_psi(psi, (char*)buffer, &p);
   cudaStream_t s = (cudaStream_t)stream;

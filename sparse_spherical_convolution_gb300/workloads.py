@@ -76,6 +76,23 @@ WORKLOADS = {
 ORDER = list(WORKLOADS)
 LARGEST = ORDER[-1]
 
+# The benchmark shapes the DISCO Kernel Development Guide lists (§benchmark
+# shapes), on Legendre-Gauss grids (poles = 2) with theta_cutoff = 0.017 and
+# kernel_shape (3, 3).  The page's "harmonic" basis and "mean" normalisation
+# are not defined there; this library's anisotropic basis (3 radial hats x
+# {1, cos, sin}, K = 9) and per-ring normalisation stand in.  B is not given:
+# 1.  The 721-row equiangular input includes the poles.  Parity-test cases,
+# not benchmark lines.
+PAGE_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("page_self_256x360x720_gauss", 1, 256, 256, (360, 720, 2), (360, 720, 2), ANISO, 3,
+                 0.017, "bf16", 5, ("fused", "fused_bwd")),
+        Workload("page_down_80x721x1440_to_360x720_gauss", 1, 80, 512, (721, 1440, 1), (360, 720, 2),
+                 ANISO, 3, 0.017, "bf16", 6, ("fwd", "bwd")),
+    ]
+}
+
 
 def make_inputs(w: Workload, with_G: bool = False, device="cpu") -> dict:
     """Seeded inputs of workload ``w`` as CPU tensors in ``w``'s dtype.

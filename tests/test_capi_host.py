@@ -55,6 +55,13 @@ def test_workspace_bytes_host_validation(lib):
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_psi_workspace_bytes((2, 8, 1), (2, 8, 1), lib.disco_basis(0, 3, 0.5))  # pole grid nlat < 3
     assert e.value.status == -1
+    # Legendre-Gauss grids (poles = 2) are accepted, from 2 rows; other grid kinds are not
+    assert lib.disco_psi_workspace_bytes((2, 8, 2), (2, 8, 2), lib.disco_basis(0, 3, 0.5)) > 0
+    assert lib.disco_psi_workspace_bytes((721, 1440, 1), (360, 720, 2), b) > 0
+    for bad in (3, -1):
+        with pytest.raises(lib.DiscoError) as e:
+            lib.disco_psi_workspace_bytes((16, 32, bad), (16, 32, 0), b)
+        assert e.value.status == -1
 
 
 def test_hot_calls_reject_unbuilt_psi_before_any_launch(lib):

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from sparse_spherical_convolution_gb300.workloads import WORKLOADS, make_inputs, sample_points
+from sparse_spherical_convolution_gb300.workloads import PAGE_WORKLOADS, WORKLOADS, make_inputs, sample_points
 from tests._helpers import TOL, rel_err, to_np32
 
 pytestmark = pytest.mark.gpu
@@ -34,6 +34,9 @@ SMALL = [
     ((10, 24, 0), (10, 12, 0), 0, 1, 0.9, 2, 3, torch.bfloat16),                  # scalar stores
     ((37, 200, 1), (37, 200, 1), 1, 3, 4 * math.pi / 36, 1, 35, torch.bfloat16),  # 4 tiles, ragged
     ((16, 31, 0), (16, 31, 0), 0, 2, 2 * math.pi / 16, 1, 3, torch.float32),      # odd width
+    ((16, 32, 2), (16, 32, 2), 1, 3, 3 * math.pi / 16, 1, 5, torch.float32),      # Legendre-Gauss
+    ((40, 128, 2), (40, 64, 2), 1, 3, 3 * math.pi / 40, 2, 70, torch.bfloat16),   # Legendre-Gauss, s = 2, tensor cores
+    ((65, 256, 1), (32, 128, 2), 1, 3, 3 * math.pi / 32, 1, 130, torch.bfloat16), # poles -> Legendre-Gauss
 ]
 
 
@@ -106,11 +109,15 @@ def _sampled_check(ref, w, inp, X, gx, n):
     assert rel_err(got, v, S) <= TOL[w.torch_dtype]
 
 
-@pytest.mark.parametrize("name", [n for n in WORKLOADS if WORKLOADS[n].grid_in[0] > 128])
+FULL = {**{n: w for n, w in WORKLOADS.items() if w.grid_in[0] > 128}, **PAGE_WORKLOADS}
+
+
+@pytest.mark.parametrize("name", list(FULL))
 def test_workload_fwd_bwd_sampled_full_size(lib, name):
-    """Full-size workloads, same launch configuration as the benchmark,
-    checked on sampled outputs (polar rows and the first/last elements included)."""
-    w = WORKLOADS[name]
+    """Full-size workloads (the benchmark's, in its launch configuration, and
+    the page's Legendre-Gauss shapes), checked on sampled outputs (polar rows
+    and the first/last elements included)."""
+    w = FULL[name]
     ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
     psi = lib.Psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
     inp = make_inputs(w, with_G=True)

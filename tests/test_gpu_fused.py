@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from sparse_spherical_convolution_gb300.workloads import WORKLOADS, make_inputs, sample_points
+from sparse_spherical_convolution_gb300.workloads import PAGE_WORKLOADS, WORKLOADS, make_inputs, sample_points
 from tests._helpers import TOL, rel_err, to_np32
 
 pytestmark = pytest.mark.gpu
@@ -117,9 +117,10 @@ def test_fused_workload_full(lib):
     assert rel_err(to_np32(y), yo, Sy) <= TOL[BF]
 
 
-@pytest.mark.parametrize("name", ["fused_bwd_361x720", "down_fused_bwd_721x1440_to_361x720"])
+@pytest.mark.parametrize("name", ["fused_bwd_361x720", "down_fused_bwd_721x1440_to_361x720",
+                                  "page_self_256x360x720_gauss"])
 def test_fused_workload_sampled_full_size(lib, name):
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if name in WORKLOADS else PAGE_WORKLOADS[name]
     inp = make_inputs(w)
     ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
     psi = lib.Psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from sparse_spherical_convolution_gb300.workloads import WORKLOADS
+from sparse_spherical_convolution_gb300.workloads import PAGE_WORKLOADS, WORKLOADS
 from tests._helpers import ulp_diff_f32
 
 pytestmark = pytest.mark.gpu
@@ -18,7 +18,9 @@ CASES = [(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff) for w in WORKLOADS.va
     ((12, 24, 0), (12, 24, 0), 1, 3, 4 * math.pi / 12),    # ties at d = cutoff on the meridian
     ((10, 24, 0), (10, 12, 0), 0, 1, 0.9),                 # K = 1, W_out not a multiple of 8
     ((16, 31, 0), (16, 31, 0), 0, 2, 2 * math.pi / 16),    # odd ring width
-]
+    ((8, 16, 2), (8, 16, 2), 0, 3, 2 * math.pi / 8),       # Legendre-Gauss grids
+    ((33, 64, 1), (16, 32, 2), 1, 3, 3 * math.pi / 16),    # pole grid -> Legendre-Gauss, s = 2
+] + [(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff) for w in PAGE_WORKLOADS.values()]
 
 
 @pytest.fixture(scope="module")
