@@ -52,7 +52,11 @@ typedef enum {
   DISCO_ERR_WORKSPACE = -7           /* workspace missing or too small */
 } disco_status;
 
-typedef enum { DISCO_F32 = 0, DISCO_BF16 = 1 } disco_dtype;
+/* Element type of the activations (x, X, G, gx, y, dy) and of W.  fp16 is
+   the page's third precision (§benchmark: "all 3 precisions (fp32, bf16,
+   fp16)"); it runs the same kernels as bf16 with fp16 operands (and fp16
+   copies of the Toeplitz tables), fp32 accumulation. */
+typedef enum { DISCO_F32 = 0, DISCO_BF16 = 1, DISCO_F16 = 2 } disco_dtype;
 
 /* Latitude rows of a grid.  poles = 0 (equiangular, midpoints): colatitude
    (i + 1/2) pi / nlat; poles = 1 (equiangular, both poles on the grid):
@@ -167,6 +171,11 @@ typedef struct {
   int32_t* grp_ptr;     /* [ngrp + 1] */
   disco_grp_ent* grp;   /* [ngrp_ent] */
   uint16_t* gtab;       /* [ngtab] */
+  /* ftab and gtab again with the values rounded to fp16 instead of bf16
+     (same offsets), for fp16 inputs: one tensor-core MMA takes A and B of
+     the same type. */
+  uint16_t* ftab_h;     /* [nftab] */
+  uint16_t* gtab_h;     /* [ngtab] */
 } disco_psi;
 
 /* Library version (major * 10000 + minor * 100 + patch). */

@@ -27,7 +27,7 @@ __all__ = [
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
-DISCO_F32, DISCO_BF16 = 0, 1
+DISCO_F32, DISCO_BF16, DISCO_F16 = 0, 1, 2
 
 EXPORTED_SYMBOLS = [
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
@@ -57,7 +57,8 @@ class disco_run(ctypes.Structure):
 
 
 _PSI_ARRAYS = ["row_ptr", "idx", "val", "csr_row_ptr", "csr_col", "csr_val", "run_ptr", "runs",
-               "trun_ptr", "truns", "hval", "row_order", "ftab_off", "ftab", "grp_ptr", "grp", "gtab"]
+               "trun_ptr", "truns", "hval", "row_order", "ftab_off", "ftab", "grp_ptr", "grp", "gtab",
+               "ftab_h", "gtab_h"]
 
 
 class disco_psi(ctypes.Structure):
@@ -143,6 +144,8 @@ def _dtype(t) -> int:
         return DISCO_F32
     if t.dtype == torch.bfloat16:
         return DISCO_BF16
+    if t.dtype == torch.float16:
+        return DISCO_F16
     raise DiscoError(-2, f"unsupported dtype {t.dtype}")
 
 
@@ -269,7 +272,8 @@ class Psi:
     _DT = {"row_ptr": "int32", "idx": "int32", "val": "float32", "csr_row_ptr": "int32",
            "csr_col": "int32", "csr_val": "float32", "run_ptr": "int32", "runs": "int32",
            "trun_ptr": "int32", "truns": "int32", "hval": "float32", "row_order": "int32",
-           "ftab_off": "int32", "ftab": "int16", "grp_ptr": "int32", "grp": "int32", "gtab": "int16"}
+           "ftab_off": "int32", "ftab": "int16", "grp_ptr": "int32", "grp": "int32", "gtab": "int16",
+           "ftab_h": "int16", "gtab_h": "int16"}
 
     def __init__(self, grid_in, grid_out, kind: int, n_radial: int, cutoff: float, stream=None):
         import torch
@@ -289,7 +293,8 @@ class Psi:
                 "csr_val": (c.nnz_csr,), "run_ptr": (Hout + 1,), "runs": (c.nruns, 8),
                 "trun_ptr": (Hin + 1,), "truns": (c.nruns,), "hval": (c.nhval, c.K_pad),
                 "row_order": (Hout,), "ftab_off": (c.nruns + 1,), "ftab": (c.nftab,),
-                "grp_ptr": (c.ngrp + 1,), "grp": (c.ngrp_ent, 4), "gtab": (c.ngtab,)}
+                "grp_ptr": (c.ngrp + 1,), "grp": (c.ngrp_ent, 4), "gtab": (c.ngtab,),
+                "ftab_h": (c.nftab,), "gtab_h": (c.ngtab,)}
 
     def tensor(self, name: str):
         """Device view of one psi array (for inspection and tests)."""

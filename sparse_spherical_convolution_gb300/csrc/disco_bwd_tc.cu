@@ -119,6 +119,7 @@ struct BtcArgs {
   int BC, Hin, Win, Hout, Wout, K;
   int ntx, nty, ntz;  // tiles along columns, channel blocks, row groups
   unsigned long long launch_id;  // selects the scheduler slot
+  int f16;                       // G, gx and the tables are fp16 (else bf16)
 };
 
 template <int S>
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kN);
+      const uint32_t idesc = idesc_16_f32(128, kN, a.f16 != 0);
       int i = 0, tl = 0;
       bool ok = true;
       for (; ok; ++tl) {
@@ -484,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w32[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-              w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+              w32[e] = pack2_16(v[2 * e], v[2 * e + 1], a.f16);
             }
             uint4* dst = reinterpret_cast<uint4*>(ob + er * 64 + cc * 32);
             dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
@@ -549,6 +549,7 @@ int sm_count() {
 // library writes itself, [K*H_out][BC][W_out] (channel rows W_out apart, which
 // lets a 128-channel box stream far faster).  Same boxes and coordinates.
 int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw, bool swz, bool rows_of_channels) {
+  const CUtensorMapDataType dt16 = a.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   auto enc = encode_fn_b();
   if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {(cuuint64_t)a.Wout, (cuuint64_t)a.K * a.Hout, (cuuint64_t)BC};
@@ -559,7 +560,7 @@ int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw
   }
   cuuint32_t box[3] = {(cuuint32_t)boxw, 1, 128};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(G), dims, strides, box, estr,
+  CUresult cr = enc(map, dt16, 3, const_cast<void*>(G), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -568,13 +569,14 @@ int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw
 }
 
 template <int S>
-int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool roc) {
+int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool roc, bool f16) {
   using Cfg = BCfg<S>;
   BtcArgs a;
   a.gx = (__nv_bfloat16*)gx;
   a.grp_ptr = psi->grp_ptr;
   a.grp = psi->grp;
-  a.gtab = psi->gtab;
+  a.gtab = f16 ? psi->gtab_h : psi->gtab;
+  a.f16 = f16 ? 1 : 0;
   a.BC = BC;
   a.Hin = psi->grid_in.nlat;
   a.Win = psi->grid_in.nlon;
@@ -595,7 +597,8 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
     cuuint64_t strides[2] = {(cuuint64_t)a.Win * 2, (cuuint64_t)a.Hin * a.Win * 2};
     cuuint32_t box[3] = {32, 1, 128};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult cr = encode_fn_b()(&gxm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, gx, dims, strides, box, estr,
+    CUresult cr = encode_fn_b()(&gxm, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                gx, dims, strides, box, estr,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
@@ -630,11 +633,12 @@ bool bwd_tc_supported(const disco_psi* psi, int BC) {
          (long long)psi->K * psi->grid_out.nlat <= (1 << 30);
 }
 
-int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool rows_of_channels) {
-  if (!bwd_tc_supported(psi, BC)) return DISCO_ERR_UNSUPPORTED;
+int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool rows_of_channels,
+                    bool f16) {
+  if (!bwd_tc_supported(psi, BC) || (f16 && !psi->gtab_h)) return DISCO_ERR_UNSUPPORTED;
   static_assert(BCfg<1>::kSmem <= 227 * 1024 && BCfg<2>::kSmem <= 227 * 1024, "shared memory");
-  return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st, rows_of_channels)
-                     : launch_btc<2>(psi, G, gx, BC, st, rows_of_channels);
+  return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st, rows_of_channels, f16)
+                     : launch_btc<2>(psi, G, gx, BC, st, rows_of_channels, f16);
 }
 
 }  // namespace disco

@@ -81,6 +81,23 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* dst, const 
     for (int t = 0; t < n; ++t) dst[t] = __float2bfloat16_rn(v[t]);
   }
 }
+template <>
+__device__ __forceinline__ void store8<__half>(__half* dst, const float* v, int n, bool vec) {
+  if (vec && n == 8) {
+    __half2 p0 = __floats2half2_rn(v[0], v[1]);
+    __half2 p1 = __floats2half2_rn(v[2], v[3]);
+    __half2 p2 = __floats2half2_rn(v[4], v[5]);
+    __half2 p3 = __floats2half2_rn(v[6], v[7]);
+    uint4 u;
+    u.x = *reinterpret_cast<uint32_t*>(&p0);
+    u.y = *reinterpret_cast<uint32_t*>(&p1);
+    u.z = *reinterpret_cast<uint32_t*>(&p2);
+    u.w = *reinterpret_cast<uint32_t*>(&p3);
+    reinterpret_cast<uint4*>(dst)[0] = u;
+  } else {
+    for (int t = 0; t < n; ++t) dst[t] = __float2half_rn(v[t]);
+  }
+}
 
 // ------------------------------------------------------------- forward --
 //
@@ -332,7 +349,7 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   if (!aligned16(in) || !aligned16(out)) return fail(DISCO_ERR_ALIGNMENT, "tensors must be 16-byte aligned");
   if (B < 1 || C < 1) return fail(DISCO_ERR_INVALID_ARG, "B and C must be >= 1");
   if ((int64_t)B * C > (int64_t)65535 * 32) return fail(DISCO_ERR_UNSUPPORTED, "B*C too large");
-  if (dtype != DISCO_F32 && dtype != DISCO_BF16) return fail(DISCO_ERR_UNSUPPORTED, "dtype");
+  if (dtype != DISCO_F32 && dtype != DISCO_BF16 && dtype != DISCO_F16) return fail(DISCO_ERR_UNSUPPORTED, "dtype");
   if (psi->s != 1 && psi->s != 2)
     return fail(DISCO_ERR_UNSUPPORTED, "W_in / W_out = %d (contractions support 1 and 2)", psi->s);
   ContractArgs a;
@@ -355,13 +372,17 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   a.vec_ok = ((fwd ? a.Wout : a.Win) % elems16) == 0;
   cudaStream_t s = (cudaStream_t)stream;
   int kind = psi->basis.kind, K = psi->K;
-  if (dtype == DISCO_BF16) {
-    // bf16: the tensor-core Toeplitz kernels where their shape rules hold
-    const int tst = fwd ? fwd_tensor_core(psi, in, out, a.BC, s) : bwd_tensor_core(psi, in, out, a.BC, s);
+  if (dtype != DISCO_F32) {
+    // bf16 / fp16: the tensor-core Toeplitz kernels where their shape rules hold
+    const bool f16 = dtype == DISCO_F16;
+    const int tst = fwd ? fwd_tensor_core(psi, in, out, a.BC, s, f16)
+                        : bwd_tensor_core(psi, in, out, a.BC, s, false, f16);
     if (tst != DISCO_ERR_UNSUPPORTED) return tst;
   }
   if (dtype == DISCO_F32)
     return psi->s == 1 ? dispatch<float, 1>(fwd, kind, K, a, s) : dispatch<float, 2>(fwd, kind, K, a, s);
+  if (dtype == DISCO_F16)
+    return psi->s == 1 ? dispatch<__half, 1>(fwd, kind, K, a, s) : dispatch<__half, 2>(fwd, kind, K, a, s);
   return psi->s == 1 ? dispatch<__nv_bfloat16, 1>(fwd, kind, K, a, s)
                      : dispatch<__nv_bfloat16, 2>(fwd, kind, K, a, s);
 }

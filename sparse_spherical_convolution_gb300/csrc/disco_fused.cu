@@ -598,7 +598,7 @@ int check_fused_common(const disco_psi* psi, const void* a, const void* W, const
   if (!a || !W || !out) return fail(DISCO_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(a) || !aligned16(W) || !aligned16(out))
     return fail(DISCO_ERR_ALIGNMENT, "tensors must be 16-byte aligned");
-  if (dtype != DISCO_BF16) return fail(DISCO_ERR_UNSUPPORTED, "fused paths take bf16 only");
+  if (dtype != DISCO_BF16 && dtype != DISCO_F16) return fail(DISCO_ERR_UNSUPPORTED, "fused paths take bf16 or fp16");
   if (B < 1 || Cin < 1 || Cout < 1) return fail(DISCO_ERR_INVALID_ARG, "B, Cin, Cout must be >= 1");
   if (B > 65535) return fail(DISCO_ERR_UNSUPPORTED, "B > 65535");
   if (psi->s != 1 && psi->s != 2)
@@ -614,11 +614,14 @@ using namespace disco;
 // Tensor-core path of disco_fused_conv: X = contraction into the workspace
 // (bf16), then the einsum on the tensor cores.
 static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y, int32_t B, int32_t Cin,
-                    int32_t Cout, void* X, cudaStream_t s) {
-  int st = fwd_tensor_core(psi, x, X, B * Cin, s);
-  if (st) return st;
+                    int32_t Cout, void* X, cudaStream_t s, bool f16) {
   const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
-  st = einsum_tensor_core(X, W, y, B, Cin * psi->K, Cout, P, s);
+  if (f16 && !(gemm_tc_supported(P, Cin * psi->K, Cout) && Cout <= 256))
+    return fail(DISCO_ERR_UNSUPPORTED, "fp16 fused conv: needs the tensor-core einsum shape "
+                "(H_out*W_out, Cin*K, Cout multiples of 8, Cin*K >= 64, 16 <= Cout <= 256)");
+  int st = fwd_tensor_core(psi, x, X, B * Cin, s, f16);
+  if (st) return st;
+  st = einsum_tensor_core(X, W, y, B, Cin * psi->K, Cout, P, s, f16);
   if (st != DISCO_ERR_UNSUPPORTED) return st;
   EinArgs e;
   e.X = (const __nv_bfloat16*)X;
@@ -639,7 +642,8 @@ static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y,
 
 extern "C" size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
                                                    disco_dtype dtype) {
-  if (!psi || B < 1 || Cin < 1 || dtype != DISCO_BF16 || !fwd_tc_supported(psi, B * Cin)) return 0;
+  if (!psi || B < 1 || Cin < 1 || (dtype != DISCO_BF16 && dtype != DISCO_F16) || !fwd_tc_supported(psi, B * Cin))
+    return 0;
   return (size_t)B * Cin * psi->K * psi->grid_out.nlat * psi->grid_out.nlon * 2;
 }
 
@@ -655,8 +659,11 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
     if (!workspace || workspace_bytes < need)
       return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     if (!aligned16(workspace)) return fail(DISCO_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-    return fused_tc(psi, x, W, y, B, Cin, Cout, workspace, s);
+    return fused_tc(psi, x, W, y, B, Cin, Cout, workspace, s, dtype == DISCO_F16);
   }
+  if (dtype == DISCO_F16)
+    return fail(DISCO_ERR_UNSUPPORTED, "fp16 fused conv: needs the tensor-core forward shape (W_in % 8 == 0, "
+                "W_in >= 64, K <= 9)");
   // shapes the tensor-core contraction does not take: X built on chip by the
   // CUDA-core gather, einsum on the tensor cores
   if (Cin % kFCC != 0) return fail(DISCO_ERR_UNSUPPORTED, "Cin must be a multiple of %d", kFCC);
@@ -683,7 +690,7 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
 
 extern "C" size_t disco_fused_conv_bwd_input_workspace_bytes(const disco_psi* psi, int32_t B,
                                                              int32_t Cin, disco_dtype dtype) {
-  if (!psi || B < 1 || Cin < 1 || dtype != DISCO_BF16) return 0;
+  if (!psi || B < 1 || Cin < 1 || (dtype != DISCO_BF16 && dtype != DISCO_F16)) return 0;
   return (size_t)B * Cin * psi->K * psi->grid_out.nlat * psi->grid_out.nlon * 2;
 }
 
@@ -705,15 +712,20 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   g.CK = Cin * psi->K;
   g.P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   cudaStream_t s = (cudaStream_t)stream;
+  const bool f16 = dtype == DISCO_F16;
   if (dx_tensor_core_supported(Cout, g.CK, g.P) && bwd_tc_supported(psi, B * Cin)) {
     // both on the tensor cores: dX goes through the workspace as
     // [K*H_out][B*Cin][W_out], whose 128-channel boxes the transpose streams
     // much faster than boxes of the [B*Cin][K][H_out][W_out] layout
     const int roc[4] = {psi->K, psi->grid_out.nlat, psi->grid_out.nlon, Cin};
-    st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s, roc);
+    st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s, roc, f16);
     if (st) return st;
-    return bwd_tensor_core(psi, workspace, gx, B * Cin, s, true);
+    return bwd_tensor_core(psi, workspace, gx, B * Cin, s, true, f16);
   }
+  if (f16)
+    return fail(DISCO_ERR_UNSUPPORTED, "fp16 fused input gradient: needs the tensor-core shapes (dX GEMM: "
+                "H_out*W_out, Cout multiples of 8, Cout >= 64, Cin*K multiple of 64; transpose: W_out % 8 == 0, "
+                "W_out >= 64, s <= 2)");
   st = dx_tensor_core(dy, W, workspace, B, Cout, g.CK, g.P, s);
   if (st == DISCO_ERR_UNSUPPORTED) {
     if (cudaFuncSetAttribute(dx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -732,7 +744,8 @@ static size_t align256z(size_t v) { return (v + 255) & ~(size_t)255; }
 
 extern "C" size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
                                                               int32_t Cout, disco_dtype dtype) {
-  if (!psi || B < 1 || Cin < 1 || Cout < 1 || dtype != DISCO_BF16 || !fwd_tc_supported(psi, B * Cin))
+  if (!psi || B < 1 || Cin < 1 || Cout < 1 || (dtype != DISCO_BF16 && dtype != DISCO_F16) ||
+      !fwd_tc_supported(psi, B * Cin))
     return 0;
   const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   const int CK = Cin * psi->K;
@@ -748,7 +761,7 @@ extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, 
   const size_t need = disco_fused_conv_bwd_weight_workspace_bytes(psi, B, Cin, Cout, dtype);
   if (need == 0)
     return fail(DISCO_ERR_UNSUPPORTED,
-                "weight gradient: needs the tensor-core forward shape (bf16, W_in % 8 == 0, W_in >= 64, "
+                "weight gradient: needs the tensor-core forward shape (bf16 or fp16, W_in % 8 == 0, W_in >= 64, "
                 "K <= 9) with H_out*W_out, Cin*K and Cout multiples of 8, Cin*K >= 64, Cout >= 16");
   if (!workspace || workspace_bytes < need) return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
@@ -757,9 +770,10 @@ extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, 
   const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   const int CK = Cin * psi->K;
   // X = the forward contraction (bf16) in the first part of the workspace
-  if ((st = fwd_tensor_core(psi, x, workspace, B * Cin, s))) return st;
+  const bool f16 = dtype == DISCO_F16;
+  if ((st = fwd_tensor_core(psi, x, workspace, B * Cin, s, f16))) return st;
   void* part = (char*)workspace + align256z((size_t)B * CK * P * 2);
-  return dw_tensor_core(dy, workspace, dW, part, B, Cout, CK, P, s);
+  return dw_tensor_core(dy, workspace, dW, part, B, Cout, CK, P, s, f16);
 }
 
 extern "C" int disco_device_status(int32_t* flags, int32_t clear) {

@@ -101,6 +101,7 @@ struct TcArgs {
   int BC, Hout, Wout, Win;
   int TLB;            // table row capacity (>= every run's row length)
   int tma_store;      // X written by TMA stores (W_out % 8 == 0 and W_out >= one tile's columns)
+  int f16;            // x, X and the tables are fp16 (else bf16)
   unsigned long long launch_id;  // selects the scheduler slot of the persistent form
 };
 
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, N);
+      const uint32_t idesc = idesc_16_f32(128, N, a.f16 != 0);
       int i = 0;
       bool ok = true;
       for (int r = r_begin; r < r_end && ok; ++r) {
@@ -391,8 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w32[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-              w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+              w32[e] = pack2_16(v[2 * e], v[2 * e + 1], a.f16);
             }
             uint4* dst = reinterpret_cast<uint4*>(smem + ((size_t)k * 128 + r) * Cfg::kOutRow + j * kTW * 2);
             dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
@@ -430,15 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t w32[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                  __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-                  w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+                  w32[e] = pack2_16(v[2 * e], v[2 * e + 1], a.f16);
                 }
                 reinterpret_cast<uint4*>(dst)[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
                 reinterpret_cast<uint4*>(dst)[1] = make_uint4(w32[4], w32[5], w32[6], w32[7]);
               } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                  if (e < n) dst[e] = __float2bfloat16_rn(v[e]);
+                  if (e < n) reinterpret_cast<uint16_t*>(dst)[e] = round_16(v[e], a.f16);
               }
             }
           }
@@ -631,7 +630,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, N);
+      const uint32_t idesc = idesc_16_f32(128, N, a.f16 != 0);
       int i = 0, tl = 0;
       bool ok = true;
       for (; ok; ++tl) {
@@ -798,8 +797,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           uint32_t w32[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            __nv_bfloat162 p2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-            w32[e] = *reinterpret_cast<uint32_t*>(&p2);
+            w32[e] = pack2_16(v[2 * e], v[2 * e + 1], a.f16);
           }
           uint4* dst = reinterpret_cast<uint4*>(pb + (size_t)er * Cfg::kOutRow + j * kTW * 2);
           dst[0] = make_uint4(w32[0], w32[1], w32[2], w32[3]);
@@ -872,8 +870,9 @@ int launch_tc_stages(const disco_psi* psi, const CUtensorMap& map, const CUtenso
 }
 
 template <int K, int S>
-int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
+int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st, bool f16) {
   constexpr size_t kMaxSmem = 227 * 1024;
+  const CUtensorMapDataType dt16 = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int Hin = psi->grid_in.nlat, Win = psi->grid_in.nlon;
   TcArgs a;
   a.X = (__nv_bfloat16*)X;
@@ -881,13 +880,14 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
   a.run_ptr = psi->run_ptr;
   a.row_order = psi->row_order;
   a.ftab_off = psi->ftab_off;
-  a.ftab = psi->ftab;
+  a.ftab = f16 ? psi->ftab_h : psi->ftab;
+  a.f16 = f16 ? 1 : 0;
   a.BC = BC;
   a.Hout = psi->grid_out.nlat;
   a.Wout = psi->grid_out.nlon;
   a.Win = Win;
   a.TLB = (Win + 16 + 7) & ~7;  // a run is at most one ring long
-  if (!psi->ftab || !psi->ftab_off) return DISCO_ERR_UNSUPPORTED;
+  if (!a.ftab || !psi->ftab_off) return DISCO_ERR_UNSUPPORTED;
   const bool fit3 = TcCfg<K, S, 3>::smem(a.TLB) <= kMaxSmem;
   const bool fit2 = TcCfg<K, S, 2>::smem(a.TLB) <= kMaxSmem;
   if (!fit2) return DISCO_ERR_UNSUPPORTED;
@@ -899,7 +899,7 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
   cuuint32_t estr[3] = {1, 1, 1};
   for (int m = 0; m < 2; ++m) {
     cuuint32_t box[3] = {m == 0 ? 64u : 8u, 1, 128};
-    CUresult cr = enc(m == 0 ? &map : &nmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims,
+    CUresult cr = enc(m == 0 ? &map : &nmap, dt16, 3, const_cast<void*>(x), dims,
                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       m == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -914,7 +914,7 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
     cuuint64_t od[3] = {(cuuint64_t)a.Wout, (cuuint64_t)K * a.Hout, (cuuint64_t)BC};
     cuuint64_t os[2] = {(cuuint64_t)a.Wout * 2, (cuuint64_t)K * a.Hout * a.Wout * 2};
     cuuint32_t ob[3] = {(cuuint32_t)(NT3 * kTW), 1, 128};
-    CUresult cr = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, X, od, os, ob, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    CUresult cr = enc(&omap, dt16, 3, X, od, os, ob, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
   }
@@ -979,12 +979,12 @@ bool fwd_tc_supported(const disco_psi* psi, int BC) {
 
 // Forward contraction on the tensor cores; returns DISCO_ERR_UNSUPPORTED
 // (without launching) for shapes this path does not take.
-int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st) {
-  if (!fwd_tc_supported(psi, BC)) return DISCO_ERR_UNSUPPORTED;
+int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st, bool f16) {
+  if (!fwd_tc_supported(psi, BC) || (f16 && !psi->ftab_h)) return DISCO_ERR_UNSUPPORTED;
   const int K = psi->K;
 #define DISCO_TCASE(KK)                                                               \
-  if (K == KK) return psi->s == 1 ? launch_tc<KK, 1>(psi, x, X, BC, st)              \
-                                  : launch_tc<KK, 2>(psi, x, X, BC, st);
+  if (K == KK) return psi->s == 1 ? launch_tc<KK, 1>(psi, x, X, BC, st, f16)         \
+                                  : launch_tc<KK, 2>(psi, x, X, BC, st, f16);
   DISCO_TCASE(1)
   DISCO_TCASE(2)
   DISCO_TCASE(3)

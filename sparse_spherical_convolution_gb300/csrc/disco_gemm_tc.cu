@@ -83,9 +83,8 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
 }
 
 // kind::f16 instruction descriptor, bf16 A and B, fp32 D; A MN-major, B as given
-__host__ __device__ constexpr uint32_t idesc_mn(int M, int N, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_mn(int M, int N, bool b_mn, bool half) {
+  return idesc_16_f32(M, N, half) | (1u << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 struct GemmTcArgs {
@@ -95,6 +94,7 @@ struct GemmTcArgs {
   // so that a TMA box of 128 channels x 64 columns of one row (k, ho) reads
   // rows W*2 bytes apart instead of a channel slab apart.
   int ctK, ctH, ctW, ctC;
+  int f16;             // operands and out are fp16 (else bf16)
   uint32_t bbytes;     // bytes of the B boxes of one stage
   int64_t P;           // pixels
   int Kt;              // reduction length j
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      const uint32_t idesc = idesc_mn(kBM, a.NB, kBMN);
+      const uint32_t idesc = idesc_mn(kBM, a.NB, kBMN, a.f16 != 0);
       int i = 0, tl = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[16];
         tmem_ld16(tmem + ab * 256 + ((uint32_t)(q * 32) << 16) + c0, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v[e]));
+        for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = round_16(v[e], a.f16);
         __syncwarp();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -330,6 +330,7 @@ struct DwArgs {
   int Cout, Nt, NB;    // rows o, columns n, columns per tile
   int mt, nt, nsplit;  // tiles along o, along n, reduction splits
   int nkp, B;          // 64-pixel chunks per image, images
+  int f16;             // dy and X are fp16 (else bf16)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, a.NB);
+      const uint32_t idesc = idesc_16_f32(kBM, a.NB, a.f16 != 0);
       int i = 0, tl = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
@@ -492,15 +493,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// dW[o][n] = bf16(sum over splits, in split order, of the partials)
-__global__ void dw_reduce_kernel(const float* part, __nv_bfloat16* dW, int Cout, int Nt, int rows, int cols,
-                                 int nsplit) {
+// dW[o][n] = bf16 or fp16 (sum over splits, in split order, of the partials)
+__global__ void dw_reduce_kernel(const float* part, uint16_t* dW, int Cout, int Nt, int rows, int cols,
+                                 int nsplit, int f16) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)Cout * Nt) return;
   const int o = (int)(i / Nt), n = (int)(i - (int64_t)o * Nt);
   float acc = 0.f;
   for (int sp = 0; sp < nsplit; ++sp) acc += part[((size_t)sp * rows + o) * cols + n];
-  dW[i] = __float2bfloat16_rn(acc);
+  dW[i] = round_16(acc, f16);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
@@ -517,11 +518,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_g() {
 }
 
 int encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-           const cuuint32_t* box) {
+           const cuuint32_t* box, bool f16) {
   auto enc = encode_fn_g();
   if (!enc) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult cr = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+  CUresult cr = enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+                    const_cast<void*>(base), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
@@ -544,8 +546,9 @@ int sm_count_g() {
 // out[b][n][p] = sum_j A[b][j][p] * Bop(j, n); W is [Nt][Kt] (kBMN false) or [Kt][Nt] (true)
 template <bool kBMN>
 int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, int64_t P, cudaStream_t st,
-                const int* ct = nullptr) {
+                const int* ct, bool f16) {
   GemmTcArgs g;
+  g.f16 = f16 ? 1 : 0;
   g.out = (__nv_bfloat16*)out;
   g.ctK = ct ? ct[0] : 0;
   g.ctH = ct ? ct[1] : 0;
@@ -565,14 +568,14 @@ int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, 
     cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)Kt, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)Kt * P * 2};
     cuuint32_t box[3] = {64, kBK, 1};
-    int s = encode(&amap, A, 3, dims, strides, box);
+    int s = encode(&amap, A, 3, dims, strides, box, f16);
     if (s) return s;
   }
   {
     cuuint64_t dims[2] = {kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt, kBMN ? (cuuint64_t)Kt : (cuuint64_t)Nt};
     cuuint64_t strides[1] = {(kBMN ? (cuuint64_t)Nt : (cuuint64_t)Kt) * 2};
     cuuint32_t box[2] = {64, kBMN ? (cuuint32_t)kBK : (cuuint32_t)(Nt < g.NB ? Nt : g.NB)};
-    int s = encode(&bmap, W, 2, dims, strides, box);
+    int s = encode(&bmap, W, 2, dims, strides, box, f16);
     if (s) return s;
   }
   auto kern = gemm_tc_kernel<kBMN>;
@@ -591,21 +594,22 @@ bool gemm_tc_supported(int64_t P, int Kt, int Nt) {
   return P % 8 == 0 && P >= 128 && Kt % 8 == 0 && Kt >= kBK && Nt % 8 == 0 && Nt >= 16;
 }
 
-int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P, cudaStream_t st) {
+int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P, cudaStream_t st,
+                       bool f16) {
   if (!gemm_tc_supported(P, CK, Cout) || Cout > 256) return DISCO_ERR_UNSUPPORTED;
-  return launch_gemm<false>(X, W, y, B, CK, Cout, P, st);
+  return launch_gemm<false>(X, W, y, B, CK, Cout, P, st, nullptr, f16);
 }
 
 bool dx_tensor_core_supported(int Cout, int CK, int64_t P) { return gemm_tc_supported(P, Cout, CK) && CK % 64 == 0; }
 
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P, cudaStream_t st,
-                   const int* rows_of_channels) {
+                   const int* rows_of_channels, bool f16) {
   if (!dx_tensor_core_supported(Cout, CK, P)) return DISCO_ERR_UNSUPPORTED;
   if (rows_of_channels) {
     const int K = rows_of_channels[0], H = rows_of_channels[1], W_ = rows_of_channels[2], C = rows_of_channels[3];
     if (K < 1 || C < 1 || W_ % 8 != 0 || (int64_t)K * C != CK || (int64_t)H * W_ != P) return DISCO_ERR_UNSUPPORTED;
   }
-  return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st, rows_of_channels);
+  return launch_gemm<true>(dy, W, dX, B, Cout, CK, P, st, rows_of_channels, f16);
 }
 
 namespace {
@@ -637,7 +641,7 @@ size_t dw_partial_bytes(int B, int Cout, int CK, int64_t P) {
 }
 
 int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int B, int Cout, int CK, int64_t P,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool f16) {
   if (!dw_tensor_core_supported(B, Cout, CK, P)) return DISCO_ERR_UNSUPPORTED;
   const DwPlan d = dw_plan(B, Cout, CK, P);
   DwArgs g;
@@ -651,6 +655,7 @@ int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int 
   g.nsplit = d.nsplit;
   g.nkp = d.nkp;
   g.B = B;
+  g.f16 = f16 ? 1 : 0;
   const int arows = Cout < kBM ? Cout : kBM, brows = CK < d.NB ? CK : d.NB;
   g.abytes = (uint32_t)arows * kBK * 2;
   g.bbytes = (uint32_t)brows * kBK * 2;
@@ -659,14 +664,14 @@ int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int 
     cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)Cout, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)Cout * P * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)arows, 1};
-    int s = encode(&amap, dy, 3, dims, strides, box);
+    int s = encode(&amap, dy, 3, dims, strides, box, f16);
     if (s) return s;
   }
   {
     cuuint64_t dims[3] = {(cuuint64_t)P, (cuuint64_t)CK, (cuuint64_t)B};
     cuuint64_t strides[2] = {(cuuint64_t)P * 2, (cuuint64_t)CK * P * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)brows, 1};
-    int s = encode(&bmap, X, 3, dims, strides, box);
+    int s = encode(&bmap, X, 3, dims, strides, box, f16);
     if (s) return s;
   }
   if (cudaFuncSetAttribute(dw_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
@@ -679,7 +684,7 @@ int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int 
   if (s) return s;
   const long long n = (long long)Cout * CK;
   dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
-      (const float*)partials, (__nv_bfloat16*)dW, Cout, CK, d.mt * kBM, d.nt * d.NB, d.nsplit);
+      (const float*)partials, (uint16_t*)dW, Cout, CK, d.mt * kBM, d.nt * d.NB, d.nsplit, f16 ? 1 : 0);
   return check_launch("dW reduce");
 }
 

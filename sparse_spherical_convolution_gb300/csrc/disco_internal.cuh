@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,7 +31,8 @@ int check_psi(const disco_psi* psi);
 
 // Forward contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
 // without launching, for shapes that path does not take.
-int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st);
+// f16: x and X are fp16 (else bf16).
+int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t st, bool f16 = false);
 bool fwd_tc_supported(const disco_psi* psi, int BC);
 
 // ORs the tensor-core unit's status word into *v (device already synchronised).
@@ -39,8 +41,9 @@ cudaError_t tc_status(int32_t* v, bool clear);
 // Transpose contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
 // without launching, for shapes that path does not take.
 // rows_of_channels: G is [K*H_out][BC][W_out] instead of [BC][K*H_out][W_out].
+// f16: G and gx are fp16 (else bf16).
 int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st,
-                    bool rows_of_channels = false);
+                    bool rows_of_channels = false, bool f16 = false);
 bool bwd_tc_supported(const disco_psi* psi, int BC);
 cudaError_t btc_status(int32_t* v, bool clear);
 
@@ -49,19 +52,21 @@ cudaError_t btc_status(int32_t* v, bool clear);
 //   dX:     dX[b][j][p] = sum_o dy[b][o][p] W[o][j]
 // DISCO_ERR_UNSUPPORTED, without launching, for shapes they do not take.
 int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P,
-                       cudaStream_t st);
+                       cudaStream_t st, bool f16 = false);
 // rows_of_channels = {K, H_out, W_out, C} (or null): write dX as
 // [K*H_out][B*C][W_out] instead of [B][C*K][P] (W_out % 8 == 0).
 bool dx_tensor_core_supported(int Cout, int CK, int64_t P);
+// Shape rule of both GEMMs: P % 8 == 0, P >= 128, Kt % 8 == 0, Kt >= 64, Nt % 8 == 0, Nt >= 16.
+bool gemm_tc_supported(int64_t P, int Kt, int Nt);
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P,
-                   cudaStream_t st, const int* rows_of_channels = nullptr);
+                   cudaStream_t st, const int* rows_of_channels = nullptr, bool f16 = false);
 cudaError_t gemm_status(int32_t* v, bool clear);
 // Weight gradient dW[o][j] = sum_b sum_p dy[b][o][p] X[b][j][p] (split reduction
 // through fp32 partials of dw_partial_bytes bytes, then rounded to bf16).
 bool dw_tensor_core_supported(int B, int Cout, int CK, int64_t P);
 size_t dw_partial_bytes(int B, int Cout, int CK, int64_t P);
 int dw_tensor_core(const void* dy, const void* X, void* dW, void* partials, int B, int Cout, int CK, int64_t P,
-                   cudaStream_t st);
+                   cudaStream_t st, bool f16 = false);
 
 // Geometry of the transpose tables by input-row group (disco_psi.grp_ptr):
 // 8 input rows per group, 64-column chunks, TQ = 32 / s decimated output
@@ -74,6 +79,7 @@ __host__ __device__ constexpr int grp_block(int s) { return kGrpRows * s * grp_c
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
 
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
@@ -82,6 +88,10 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
+}
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) {
+  return __float2half_rn(v);
 }
 
 }  // namespace disco

@@ -306,6 +306,8 @@ struct PsiOut {
   int32_t* grp_ptr;
   disco_grp_ent* grp;
   uint16_t* gtab;
+  uint16_t* ftab_h;  // the same tables rounded to fp16
+  uint16_t* gtab_h;
 };
 
 __device__ __forceinline__ int ring_of(int kind, int k) { return kind == 1 ? k / 3 : k; }
@@ -469,6 +471,7 @@ __global__ void table_kernel(PsiGeom g, Workspace ws, PsiOut p) {
       const int d = dlo + x - 8;
       const float v = (d >= dlo && d <= dhi) ? p.val[(size_t)(e0 + d - dlo) * g.Kp + k] : 0.f;
       p.ftab[foff + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      p.ftab_h[foff + i] = __half_as_ushort(__float2half_rn(v));
     }
   }
 }
@@ -569,6 +572,7 @@ __global__ void gfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
         }
       }
       p.gtab[(size_t)en.off + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      p.gtab_h[(size_t)en.off + i] = __half_as_ushort(__float2half_rn(v));
     }
   }
 }
@@ -676,6 +680,8 @@ size_t carve_psi(const disco_psi* psi, char* base, PsiOut* out) {
   p.grp_ptr = (int32_t*)take((size_t)(psi->ngrp + 1) * 4);
   p.grp = (disco_grp_ent*)take((size_t)psi->ngrp_ent * sizeof(disco_grp_ent));
   p.gtab = (uint16_t*)take((size_t)psi->ngtab * 2);
+  p.ftab_h = (uint16_t*)take((size_t)psi->nftab * 2);
+  p.gtab_h = (uint16_t*)take((size_t)psi->ngtab * 2);
   if (out) *out = p;
   return o;
 }
@@ -844,5 +850,7 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   psi->grp_ptr = p.grp_ptr;
   psi->grp = p.grp;
   psi->gtab = p.gtab;
+  psi->ftab_h = p.ftab_h;
+  psi->gtab_h = p.gtab_h;
   return DISCO_OK;
 }

@@ -119,14 +119,29 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4)            // D format: f32
-         | (1u << 7)          // A format: bf16
-         | (1u << 10)         // B format: bf16
-         | (0u << 15)         // A K-major
-         | (0u << 16)         // B K-major
+// Instruction descriptor, kind::f16: A and B both fp16 (half) or both bf16,
+// fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, bool half) {
+  return (1u << 4)                    // D format: f32
+         | ((half ? 0u : 1u) << 7)    // A format: f16 / bf16
+         | ((half ? 0u : 1u) << 10)   // B format: f16 / bf16
+         | (0u << 15)                 // A K-major
+         | (0u << 16)                 // B K-major
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) { return idesc_16_f32(M, N, false); }
+
+// Two fp32 values rounded (to nearest even) to a packed pair of fp16 or bf16.
+__device__ __forceinline__ uint32_t pack2_16(float lo, float hi, bool half) {
+  if (half) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ uint16_t round_16(float v, bool half) {
+  return half ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

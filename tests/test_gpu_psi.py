@@ -113,22 +113,30 @@ def _bf16_bits(v):
     return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
 
 
+def _f16_bits(v):
+    return torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(torch.float16).view(torch.int16).numpy()
+
+
 def _check_tables(psi, runs, val, gi, go):
     """Forward tables and the transpose tables by input-row group hold exactly
-    the bf16-rounded union values at the documented positions, zeros elsewhere."""
+    the bf16-rounded union values at the documented positions, zeros elsewhere;
+    their fp16 copies the fp16-rounded values at the same positions."""
     K, W, s = psi.c.K, gi[1], gi[1] // go[1]
     ftab, foff = psi.tensor("ftab").cpu().numpy(), psi.tensor("ftab_off").cpu().numpy()
+    ftab_h = psi.tensor("ftab_h").cpu().numpy()
     assert foff[-1] == psi.c.nftab
     ext = {}
     for r, (ho, hi, D, hoff, e0, ln, npair, anti) in enumerate(runs):
         dlo = -(W // 2) if ln == W else -npair
         dhi = dlo + ln - 1
         vb = _bf16_bits(val[e0:e0 + ln, :K])            # [len, K], offsets dlo..dhi
-        ext[(int(ho), int(hi))] = (dlo, dhi, vb)
+        vh = _f16_bits(val[e0:e0 + ln, :K])
+        ext[(int(ho), int(hi))] = (dlo, dhi, vb, vh)
         TL = (ln + 16 + 7) // 8 * 8
-        want = np.zeros((K, TL), np.int16)
-        want[:, 8:8 + ln] = vb.T
-        assert np.array_equal(ftab[foff[r]:foff[r] + K * TL].reshape(K, TL), want)
+        for tab, v in ((ftab, vb), (ftab_h, vh)):
+            want = np.zeros((K, TL), np.int16)
+            want[:, 8:8 + ln] = v.T
+            assert np.array_equal(tab[foff[r]:foff[r] + K * TL].reshape(K, TL), want)
     _check_group_tables(psi, ext, gi, go)
 
 
@@ -153,6 +161,7 @@ def _check_group_tables(psi, ext, gi, go):
     gptr = psi.tensor("grp_ptr").cpu().numpy()
     grp = psi.tensor("grp").cpu().numpy()
     gtab = psi.tensor("gtab").cpu().numpy()
+    gtab_h = psi.tensor("gtab_h").cpu().numpy()
     assert gptr[0] == 0 and gptr[-1] == psi.c.ngrp_ent
     assert psi.c.grp_max == int(np.diff(gptr).max())
     off_next = 0
@@ -164,23 +173,26 @@ def _check_group_tables(psi, ext, gi, go):
         for e in ents:
             ho, off = int(e[0]), int(e[1])
             MW, KB, nch = int(e[2]) & 0xFFFF, int(e[2]) >> 16, int(e[3]) & 0xFFFF
-            E = max(_halfwidth(dlo, dhi, s) for (h2, hi), (dlo, dhi, _) in ext.items()
+            E = max(_halfwidth(dlo, dhi, s) for (h2, hi), (dlo, dhi, _, _) in ext.items()
                     if h2 == ho and hi in rows)
             assert MW == (E + 7) // 8 * 8
             assert KB == (TQ + 2 * MW + 15) // 16 and nch == (KB + 3) // 4
             assert off == off_next
             off_next += K * nch * BLK
-            want = np.zeros((K, nch, 8, s, CW), np.int16)
+            want_b = np.zeros((K, nch, 8, s, CW), np.int16)
+            want_h = np.zeros((K, nch, 8, s, CW), np.int16)
             for r, hi in enumerate(rows):
                 if (ho, hi) not in ext:
                     continue
-                dlo, dhi, vb = ext[(ho, hi)]
+                dlo, dhi, vb, vh = ext[(ho, hi)]
                 for c in range(nch):
                     for p in range(s):
                         y = np.arange(CW)
                         d = s * (MW + TQ - 1 - 64 * c - y) + p
                         ok = (d >= dlo) & (d <= dhi)
-                        want[:, c, r, p, y[ok]] = vb[d[ok] - dlo].T
-            got = gtab[off:off + K * nch * BLK].reshape(K, nch, 8, s, CW)
-            assert np.array_equal(got, want), (z, ho)
+                        want_b[:, c, r, p, y[ok]] = vb[d[ok] - dlo].T
+                        want_h[:, c, r, p, y[ok]] = vh[d[ok] - dlo].T
+            for t, (tab, want) in enumerate(((gtab, want_b), (gtab_h, want_h))):
+                got = tab[off:off + K * nch * BLK].reshape(K, nch, 8, s, CW)
+                assert np.array_equal(got, want), (z, ho, t)
     assert off_next == psi.c.ngtab
