@@ -206,6 +206,20 @@ DISCO_API int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_o
 DISCO_API int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* Init time, asynchronous.  Writes a built psi in the page's uniform
+   K-packed form (§kpacked layout), for interoperability with code that reads
+   that form:
+     pack_idx   [H_out][nbr_pad][2]      int64 (hi, wi), shared across k
+     pack_val   [H_out][nbr_pad][K_pad]  fp32, zero for k >= K
+     pack_count [H_out]                  int64, neighbours of row ho
+   Row ho holds the union entries of output row ho in the union layout's
+   order (hi ascending, then signed offset); entries at and past
+   pack_count[ho] are (0, 0) with zero values.  nbr_pad >= psi->max_row
+   (DISCO_ERR_INVALID_ARG otherwise); all three are caller-owned device
+   buffers, fully overwritten. */
+DISCO_API int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, float* pack_val,
+                                       int64_t* pack_count, int32_t nbr_pad, void* stream);
+
 /* Forward S2 contraction (§Architecture snapshot "forward"; §Backward
    direction: gather, each output pixel reads a bounded neighbourhood):
      X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]

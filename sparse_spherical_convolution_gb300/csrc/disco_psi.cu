@@ -619,6 +619,24 @@ __global__ void order_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   p.row_order[rank] = ho;
 }
 
+// The page's uniform K-packed form of the union layout; one block per output row.
+__global__ void export_kpacked_kernel(const int32_t* row_ptr, const int32_t* idx, const float* val, int Kp,
+                                      int nbr_pad, int64_t* pidx, float* pval, int64_t* pcount) {
+  const int ho = blockIdx.x;
+  const int e0 = row_ptr[ho], n = row_ptr[ho + 1] - e0;
+  if (threadIdx.x == 0) pcount[ho] = n;
+  const int64_t base = (int64_t)ho * nbr_pad;
+  for (int j = threadIdx.x; j < nbr_pad; j += blockDim.x) {
+    const bool in = j < n;
+    pidx[(base + j) * 2] = in ? idx[(size_t)(e0 + j) * 2] : 0;
+    pidx[(base + j) * 2 + 1] = in ? idx[(size_t)(e0 + j) * 2 + 1] : 0;
+  }
+  for (int64_t t = threadIdx.x; t < (int64_t)nbr_pad * Kp; t += blockDim.x) {
+    const int j = (int)(t / Kp), k = (int)(t - (int64_t)j * Kp);
+    pval[base * Kp + t] = j < n ? val[(size_t)(e0 + j) * Kp + k] : 0.f;
+  }
+}
+
 int make_geom(const disco_grid* gi, const disco_grid* go, const disco_basis* b, PsiGeom* g) {
   if (!gi || !go || !b) return fail(DISCO_ERR_INVALID_ARG, "null grid or basis");
   if (gi->nlat < 2 || go->nlat < 2 || gi->nlon < 1 || go->nlon < 1)
@@ -853,4 +871,20 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   psi->ftab_h = p.ftab_h;
   psi->gtab_h = p.gtab_h;
   return DISCO_OK;
+}
+
+extern "C" int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, float* pack_val,
+                                        int64_t* pack_count, int32_t nbr_pad, void* stream) {
+  int st = check_psi(psi);
+  if (st) return st;
+  if ((st = check_device())) return st;
+  if (!pack_idx || !pack_val || !pack_count) return fail(DISCO_ERR_INVALID_ARG, "null output pointer");
+  if ((reinterpret_cast<uintptr_t>(pack_idx) & 7u) || (reinterpret_cast<uintptr_t>(pack_count) & 7u) ||
+      (reinterpret_cast<uintptr_t>(pack_val) & 3u))
+    return fail(DISCO_ERR_ALIGNMENT, "outputs must be aligned to their element size");
+  if (nbr_pad < 1 || nbr_pad < psi->max_row)
+    return fail(DISCO_ERR_INVALID_ARG, "nbr_pad (%d) must be >= max_row (%d)", nbr_pad, psi->max_row);
+  export_kpacked_kernel<<<psi->grid_out.nlat, 256, 0, (cudaStream_t)stream>>>(
+      psi->row_ptr, psi->idx, psi->val, psi->K_pad, nbr_pad, pack_idx, pack_val, pack_count);
+  return check_launch("psi kpacked export");
 }

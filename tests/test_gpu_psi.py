@@ -196,3 +196,34 @@ def _check_group_tables(psi, ext, gi, go):
                 got = tab[off:off + K * nch * BLK].reshape(K, nch, 8, s, CW)
                 assert np.array_equal(got, want), (z, ho, t)
     assert off_next == psi.c.ngtab
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[3], CASES[-1]], ids=lambda c: f"{c[0]}->{c[1]}")
+def test_export_uniform_kpacked(lib, case):
+    """The page's uniform K-packed form: counts and indices bit-exact against
+    the oracle's union layout, values bit-exact against the built union
+    values, zero padding, and nbr_pad < max_row rejected."""
+    gi, go, kind, nrad, cut = case
+    ref = oracle.build_psi(gi, go, kind, nrad, cut)
+    psi = lib.Psi(gi, go, kind, nrad, cut)
+    Ho, Kp = go[0], psi.c.K_pad
+    counts = np.diff(ref.row_ptr)
+    assert psi.c.max_row == counts.max()
+    val = psi.tensor("val").cpu().numpy()
+    for pad in (int(counts.max()), int(counts.max()) + 5):
+        pidx = torch.full((Ho, pad, 2), -7, dtype=torch.int64, device="cuda")
+        pval = torch.full((Ho, pad, Kp), float("nan"), dtype=torch.float32, device="cuda")
+        pcnt = torch.full((Ho,), -7, dtype=torch.int64, device="cuda")
+        lib.disco_psi_export_kpacked(psi.c, pidx, pval, pcnt, pad)
+        torch.cuda.synchronize()
+        pidx, pval, pcnt = pidx.cpu().numpy(), pval.cpu().numpy(), pcnt.cpu().numpy()
+        assert np.array_equal(pcnt, counts)
+        for ho in range(Ho):
+            lo, hi_, n = ref.row_ptr[ho], ref.row_ptr[ho + 1], counts[ho]
+            assert np.array_equal(pidx[ho, :n], ref.idx[lo:hi_])
+            assert np.array_equal(pval[ho, :n], val[lo:hi_])
+            assert not pidx[ho, n:].any() and not pval[ho, n:].any()
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_psi_export_kpacked(psi.c, pidx_d := torch.zeros(1, dtype=torch.int64, device="cuda"),
+                                     torch.zeros(1, device="cuda"), pidx_d, int(counts.max()) - 1)
+    assert e.value.status == -1
