@@ -339,10 +339,20 @@ DISCO_API int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, c
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,
    bit 2 = one of the tensor-core forward contraction timed out,
    bit 3 = one of the tensor-core transpose contraction timed out or met an
-   input-row group reading more output rows than it can hold; a
-   kernel that times out stops issuing work, frees its tensor memory and
-   returns, leaving its outputs incomplete).  clear != 0 resets the word. */
+   input-row group reading more output rows than it can hold, bit 4 = the
+   wait of disco_check_wait_timeout ran out; a kernel that times out stops
+   issuing work, frees its tensor memory and returns, leaving its outputs
+   incomplete).  clear != 0 resets the word. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
+
+/* Diagnostic of the failure path, asynchronous: launches one small kernel
+   whose thread waits on an mbarrier phase that nothing completes, with the
+   bounded wait the tensor-core kernels use (`limit` polls, 1 <= limit <=
+   2^24).  When the wait runs out the kernel sets bit 4 of the device status
+   word and returns: nothing faults, traps or hangs, and the context stays
+   usable.  Lets a test check that a timed-out wait reaches
+   disco_device_status. */
+DISCO_API int disco_check_wait_timeout(uint32_t limit, void* stream);
 
 #ifdef __cplusplus
 }

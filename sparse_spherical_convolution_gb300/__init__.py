@@ -18,7 +18,7 @@ from . import build as _build_mod
 __all__ = [
     "DiscoError", "disco_grid", "disco_basis", "disco_run", "disco_psi", "Psi",
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
-    "disco_build_psi_kpacked", "disco_psi_export_kpacked", "disco_fwd", "disco_bwd",
+    "disco_build_psi_kpacked", "disco_psi_export_kpacked", "disco_check_wait_timeout", "disco_fwd", "disco_bwd",
     "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = [
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
     "disco_fused_conv_bwd_weight", "disco_device_status", "disco_psi_export_kpacked",
+    "disco_check_wait_timeout",
 ]
 
 
@@ -101,6 +102,8 @@ def load_library():
     lib.disco_psi_plan.argtypes = [PG, PG, PB, P, SZ, P, PP]
     lib.disco_build_psi_kpacked.restype = ctypes.c_int
     lib.disco_build_psi_kpacked.argtypes = [PP, P, SZ, P, SZ, P]
+    lib.disco_check_wait_timeout.restype = ctypes.c_int
+    lib.disco_check_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.disco_psi_export_kpacked.restype = ctypes.c_int
     lib.disco_psi_export_kpacked.argtypes = [PP, P, P, P, I32, P]
     lib.disco_fwd.restype = ctypes.c_int
@@ -201,6 +204,10 @@ def disco_build_psi_kpacked(psi: disco_psi, buffer, workspace, stream=None) -> N
     _check(load_library().disco_build_psi_kpacked(
         ctypes.byref(psi), _ptr(buffer), buffer.numel() * buffer.element_size(), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def disco_check_wait_timeout(limit: int, stream=None) -> None:
+    _check(load_library().disco_check_wait_timeout(limit, _stream(stream)))
 
 
 def disco_psi_export_kpacked(psi: disco_psi, pack_idx, pack_val, pack_count, nbr_pad: int,

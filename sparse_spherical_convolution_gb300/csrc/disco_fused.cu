@@ -42,7 +42,7 @@ __device__ int g_device_status = 0;
 namespace {
 
 constexpr uint32_t kWaitLimit = 1u << 24;  // polls before an mbarrier wait gives up
-enum : int { kStatusFusedTimeout = 1, kStatusGemmTimeout = 2 };
+enum : int { kStatusFusedTimeout = 1, kStatusGemmTimeout = 2, kStatusWaitCheck = 16 };
 
 __device__ __forceinline__ void flag_status(int bit) { atomicOr(&g_device_status, bit); }
 
@@ -774,6 +774,25 @@ extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, 
   if ((st = fwd_tensor_core(psi, x, workspace, B * Cin, s, f16))) return st;
   void* part = (char*)workspace + align256z((size_t)B * CK * P * 2);
   return dw_tensor_core(dy, workspace, dW, part, B, Cout, CK, P, s, f16);
+}
+
+// One thread waits, with the bounded wait of the tensor-core kernels, on the
+// first phase of an mbarrier that nothing arrives on; when the wait runs out
+// it records that in the status word and returns.
+__global__ void wait_check_kernel(uint32_t limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, limit)) flag_status(kStatusWaitCheck);
+}
+
+extern "C" int disco_check_wait_timeout(uint32_t limit, void* stream) {
+  int st = check_device();
+  if (st) return st;
+  if (limit < 1 || limit > (1u << 24)) return fail(DISCO_ERR_INVALID_ARG, "limit must be in [1, 2^24]");
+  wait_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit);
+  return check_launch("wait check");
 }
 
 extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
