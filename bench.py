@@ -105,6 +105,18 @@ def _dist():
     return ws, rank, local
 
 
+def _max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks (the job's time is the
+    slowest rank's); the values themselves on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def algorithmic(w, psi_c):
     """Compulsory bytes and useful flops per call (see the design notes)."""
     esz = 2 if w.dtype == "bf16" else 4
@@ -198,10 +210,7 @@ def run_ours(args):
     per = {name: [evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)]
            for i, (name, _) in enumerate(calls)}
     contr_ms = sum(per["fwd"]) + sum(per["bwd"])
-    if ws > 1:
-        tt = torch.tensor([total_ms, contr_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms, contr_ms = float(tt[0]), float(tt[1])
+    total_ms, contr_ms = _max_over_ranks([total_ms, contr_ms], dev)
     if d.disco_device_status() != 0:
         raise RuntimeError("a bounded wait timed out during the timed region")
 
@@ -262,10 +271,7 @@ def run_ours(args):
         a1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a0.elapsed_time(a1) / ne
-        if ws > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt[0])
+        e2e_ms = _max_over_ranks([e2e_ms], dev)[0]
         e2e = {"value": round(ws * (alg["fwd_bytes"] + alg["bwd_bytes"]) / (e2e_ms * 1e6), 2),
                "unit": "GB/s",
                "h2d_bytes_per_step": x.numel() * x.element_size() + G.numel() * G.element_size(),
@@ -342,17 +348,19 @@ def _traffic_from_profiles(kernel: str, workload: str):
         return None
 
 
-def cpu_baseline(w, budget_s: float):
+def cpu_baseline(w, budget_s: float, ref=None):
     """The fp64 oracle, as it stands, on a bounded sample of the workload:
     the forward and transpose contractions over the first n channels (n =
-    host cores, one OpenMP thread each), scaled to the same GB/s metric."""
+    host cores, one OpenMP thread each), scaled to the same GB/s metric.
+    `ref` is the oracle's psi for the workload (built here when None; the
+    build is init work, outside the timed sample)."""
     import numpy as np
     import torch
     import oracle
-    from sparse_spherical_convolution_gb300.workloads import WORKLOADS  # noqa: F401
 
     cores = os.cpu_count() or 1
-    ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
+    if ref is None:
+        ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
     g = torch.Generator().manual_seed(w.seed)
     Hin, Win = w.grid_in[:2]
     Hout, Wout = w.grid_out[:2]
@@ -378,14 +386,16 @@ def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
+    import oracle
     from sparse_spherical_convolution_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
     vals = []
     cb = None
     for _ in range(args.warmup):
-        cpu_baseline(w, args.cpu_budget_s)
+        cpu_baseline(w, args.cpu_budget_s, ref)
     for _ in range(args.steps):
-        cb = cpu_baseline(w, args.cpu_budget_s)
+        cb = cpu_baseline(w, args.cpu_budget_s, ref)
         vals.append(cb["value"])
     v = statistics.median(vals)
     out = {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
