@@ -334,6 +334,28 @@ DISCO_API int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, c
                                           int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
                                           void* workspace, size_t workspace_bytes, void* stream);
 
+/* Host-buffer forms of disco_fwd / disco_bwd for data that lives in host
+   memory: `in_host` and `out_host` are HOST pointers (page-locked memory
+   lets the copies overlap the kernels; pageable memory works, with the
+   copies staged by the runtime).  The B*C planes go in blocks of 128: each
+   block's host-to-device copy, contraction (on `stream`) and device-to-host
+   copy are ordered by events, and consecutive blocks overlap (block i+1 is
+   copied in and block i-1 copied out while block i computes).  The copies
+   run on two streams the library creates once per device and shares between
+   calls, so calls on different caller streams also overlap one another.
+   Staging (two slots of one block's input and output) is the caller's
+   device workspace of disco_host_workspace_bytes bytes, 256-byte aligned.
+   Asynchronous: `stream` waits for the last copy-out, so synchronising
+   `stream` makes out_host readable.  Same results as the device forms, bit
+   for bit; the same shape and dtype rules.  forward != 0: sizes for
+   disco_fwd_host, else disco_bwd_host (0 for invalid arguments). */
+DISCO_API size_t disco_host_workspace_bytes(const disco_psi* psi, int32_t B, int32_t C, int32_t forward,
+                                            disco_dtype dtype);
+DISCO_API int disco_fwd_host(const disco_psi* psi, const void* x_host, void* X_host, int32_t B, int32_t C,
+                             disco_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+DISCO_API int disco_bwd_host(const disco_psi* psi, const void* G_host, void* gx_host, int32_t B, int32_t C,
+                             disco_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Diagnostics; BLOCKS the host (synchronises the current device).  Reads
    the device status word into *flags (0 = no fault; bit 0 = an mbarrier wait
    of the fused forward timed out, bit 1 = one of the dX GEMM timed out,

@@ -19,6 +19,7 @@ __all__ = [
     "DiscoError", "disco_grid", "disco_basis", "disco_run", "disco_psi", "Psi",
     "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_psi_export_kpacked", "disco_check_wait_timeout", "disco_fwd", "disco_bwd",
+    "disco_host_workspace_bytes", "disco_fwd_host", "disco_bwd_host",
     "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = [
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
     "disco_fused_conv_bwd_weight", "disco_device_status", "disco_psi_export_kpacked",
-    "disco_check_wait_timeout",
+    "disco_check_wait_timeout", "disco_host_workspace_bytes", "disco_fwd_host", "disco_bwd_host",
 ]
 
 
@@ -102,6 +103,11 @@ def load_library():
     lib.disco_psi_plan.argtypes = [PG, PG, PB, P, SZ, P, PP]
     lib.disco_build_psi_kpacked.restype = ctypes.c_int
     lib.disco_build_psi_kpacked.argtypes = [PP, P, SZ, P, SZ, P]
+    lib.disco_host_workspace_bytes.restype = SZ
+    lib.disco_host_workspace_bytes.argtypes = [PP, I32, I32, I32, ctypes.c_int]
+    for nm in ("disco_fwd_host", "disco_bwd_host"):
+        getattr(lib, nm).restype = ctypes.c_int
+        getattr(lib, nm).argtypes = [PP, P, P, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_check_wait_timeout.restype = ctypes.c_int
     lib.disco_check_wait_timeout.argtypes = [ctypes.c_uint32, P]
     lib.disco_psi_export_kpacked.restype = ctypes.c_int
@@ -204,6 +210,24 @@ def disco_build_psi_kpacked(psi: disco_psi, buffer, workspace, stream=None) -> N
     _check(load_library().disco_build_psi_kpacked(
         ctypes.byref(psi), _ptr(buffer), buffer.numel() * buffer.element_size(), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def disco_host_workspace_bytes(psi: disco_psi, B: int, C: int, forward: bool, dtype=DISCO_BF16) -> int:
+    return load_library().disco_host_workspace_bytes(ctypes.byref(psi), B, C, 1 if forward else 0, dtype)
+
+
+def disco_fwd_host(psi: disco_psi, x_host, X_host, B: int, C: int, workspace, stream=None) -> None:
+    """x_host, X_host: CPU tensors (pinned for overlap); workspace: device."""
+    _check(load_library().disco_fwd_host(ctypes.byref(psi), _ptr(x_host), _ptr(X_host), B, C, _dtype(x_host),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
+
+
+def disco_bwd_host(psi: disco_psi, G_host, gx_host, B: int, C: int, workspace, stream=None) -> None:
+    """G_host, gx_host: CPU tensors (pinned for overlap); workspace: device."""
+    _check(load_library().disco_bwd_host(ctypes.byref(psi), _ptr(G_host), _ptr(gx_host), B, C, _dtype(G_host),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
 
 
 def disco_check_wait_timeout(limit: int, stream=None) -> None:

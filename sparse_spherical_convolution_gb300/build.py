@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, f"libdisco_gb300_{platform.machine()}.so")
 SOURCES = ["disco_capi.cu", "disco_psi.cu", "disco_contract.cu", "disco_fused.cu",
-           "disco_fwd_tc.cu", "disco_bwd_tc.cu", "disco_gemm_tc.cu"]
+           "disco_fwd_tc.cu", "disco_bwd_tc.cu", "disco_gemm_tc.cu", "disco_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
