@@ -225,10 +225,10 @@ DISCO_API int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, 
      X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]
                         * x[b,c,hi,(wi + wo*s) mod W_in]
    x: [B, C, H_in, W_in], X: [B, C, K, H_out, W_out], both `dtype`.
-   Supports s in {1, 2}.  bf16 with W_in % 8 == 0, W_in >= 64 and K <= 9
-   runs on the tensor cores (banded Toeplitz tiles of the run windows, fp32
-   accumulation in tensor memory); fp32, and other bf16 shapes, run the
-   CUDA-core gather. */
+   Supports s in {1, 2}.  bf16 or fp16 with W_in % 8 == 0, W_in >= 64 and
+   K <= 9 runs on the tensor cores (banded Toeplitz tiles of the run windows,
+   fp32 accumulation in tensor memory); fp32, and other bf16 / fp16 shapes,
+   run the CUDA-core gather. */
 DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
@@ -239,17 +239,17 @@ DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B,
                        psi[k,ho,hi,wi0] * G[b,c,k,ho,wo]
    G: [B, C, K, H_out, W_out], gx: [B, C, H_in, W_in], both `dtype`.
    Each output element has one owner (latitude-row ownership, no atomics).
-   bf16 with W_in and W_out multiples of 8, W_out >= 64 and K <= 16 runs on
-   the tensor cores (polyphase Toeplitz tiles, 8 input rows per tile sharing
-   each G window, psi from the tables by input-row group); other cases run the
-   CUDA-core gather. */
+   bf16 or fp16 with W_in and W_out multiples of 8, W_out >= 64 and K <= 16
+   runs on the tensor cores (polyphase Toeplitz tiles, 8 input rows per tile
+   sharing each G window, psi from the tables by input-row group); other
+   cases run the CUDA-core gather. */
 DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
-/* Device workspace bytes of disco_fused_conv: the bf16 intermediate
-   X[B, Cin, K, H_out, W_out] when the tensor-core contraction takes the shape
-   (bf16, W_in % 8 == 0, W_in >= 64, s in {1, 2}, K <= 9), else 0 (no
-   workspace needed). */
+/* Device workspace bytes of disco_fused_conv: the intermediate
+   X[B, Cin, K, H_out, W_out] (dtype) when the tensor-core contraction takes
+   the shape (bf16 or fp16, W_in % 8 == 0, W_in >= 64, s in {1, 2}, K <= 9),
+   else 0 (no workspace needed). */
 DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
                                                   disco_dtype dtype);
 
@@ -257,29 +257,40 @@ DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t 
    contraction + einsum"):  y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo]
    with X the forward contraction, in one call:
      - where the tensor-core contraction takes the shape, X is produced by it
-       into `workspace` (bf16, disco_fused_conv_workspace_bytes bytes) and the
+       into `workspace` (disco_fused_conv_workspace_bytes bytes) and the
        einsum runs as a tcgen05 GEMM (M = 128 pixels, N = Cout, K = Cin*K);
-     - otherwise X is built in shared memory by the CUDA-core gather, 16 input
-       channels at a time, and contracted on the tcgen05 tensor cores without
-       leaving the chip (workspace unused; needs Cin % 16 == 0).
-   Accumulation is fp32 (TMEM); X is rounded to bf16 before the einsum.
-   x: [B, Cin, H_in, W_in] bf16, W: [Cout, Cin, K] bf16, y: [B, Cout, H_out, W_out] bf16.
-   dtype must be DISCO_BF16; Cout <= 256. */
+     - otherwise (bf16 only) X is built in shared memory by the CUDA-core
+       gather, 16 input channels at a time, and contracted on the tcgen05
+       tensor cores without leaving the chip (workspace unused; needs
+       Cin % 16 == 0).
+   Accumulation is fp32 (TMEM); X is rounded to the dtype before the einsum.
+   x: [B, Cin, H_in, W_in], W: [Cout, Cin, K], y: [B, Cout, H_out, W_out],
+   all bf16 or all fp16 (dtype); Cout <= 256.  fp16 needs the tensor-core
+   path: the forward shape above and the GEMM shape (H_out*W_out, Cin*K and
+   Cout multiples of 8, Cin*K >= 64, Cout >= 16); else DISCO_ERR_UNSUPPORTED
+   before any launch. */
 DISCO_API int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
                      int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
                      void* workspace, size_t workspace_bytes, void* stream);
 
-/* Device workspace bytes of disco_fused_conv_bwd_input (the bf16 intermediate
-   dX[B, Cin, K, H_out, W_out]). */
+/* Device workspace bytes of disco_fused_conv_bwd_input (the intermediate dX,
+   B * Cin * K * H_out * W_out elements of the dtype). */
 DISCO_API size_t disco_fused_conv_bwd_input_workspace_bytes(const disco_psi* psi, int32_t B,
                                                   int32_t Cin, disco_dtype dtype);
 
 /* Input gradient of the fused convolution:
      dX[b,c,k,ho,wo] = sum_o W[o,c,k] dy[b,o,ho,wo]   (tcgen05 tensor cores)
      gx = psi^T dX                                    (the transpose contraction)
-   dy: [B, Cout, H_out, W_out] bf16, W: [Cout, Cin, K] bf16, gx: [B, Cin, H_in, W_in] bf16.
-   dX is kept in `workspace` (>= disco_fused_conv_bwd_input_workspace_bytes)
-   as bf16.  dtype must be DISCO_BF16; Cout % 16 == 0. */
+   dy: [B, Cout, H_out, W_out], W: [Cout, Cin, K], gx: [B, Cin, H_in, W_in],
+   all bf16 or all fp16 (dtype).  dX is kept in `workspace` (>=
+   disco_fused_conv_bwd_input_workspace_bytes) in the dtype: as
+   [K*H_out][B*Cin][W_out] when both steps run on the tensor cores (dX GEMM:
+   H_out*W_out and Cout multiples of 8, Cout >= 64, Cin*K a multiple of 64;
+   transpose: the disco_bwd tensor-core shape), whose 128-channel windows the
+   transpose streams faster than those of [B][Cin*K][H_out*W_out], the
+   layout of the other cases (bf16 only: a CUDA-core dX GEMM, then
+   disco_bwd).  fp16 needs the tensor-core shapes, else DISCO_ERR_UNSUPPORTED
+   before any launch. */
 DISCO_API int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, const void* W,
                                void* gx, int32_t B, int32_t Cin, int32_t Cout,
                                disco_dtype dtype, void* workspace, size_t workspace_bytes,
@@ -309,7 +320,7 @@ DISCO_API int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const voi
                                                  int32_t Cin, int32_t Cout, disco_dtype dtype,
                                                  void* stream);
 
-/* Device workspace bytes of disco_fused_conv_bwd_weight: X (bf16) plus the
+/* Device workspace bytes of disco_fused_conv_bwd_weight: X (dtype) plus the
    fp32 partial sums of the split reduction; 0 when the call does not take the
    shape (see below). */
 DISCO_API size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* psi, int32_t B,
@@ -322,11 +333,11 @@ DISCO_API size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* ps
      dW[o,c,k] = sum_b sum_{ho,wo} dy[b,o,ho,wo] X[b,c,k,ho,wo],
    X the forward contraction of x (recomputed, not stored by the forward).
    x: [B, Cin, H_in, W_in], dy: [B, Cout, H_out, W_out], dW: [Cout, Cin, K],
-   all bf16 (dW rounded from an fp32 sum).  X is built by the tensor-core
+   all bf16 or all fp16 (dW rounded from an fp32 sum).  X is built by the tensor-core
    contraction into `workspace` (>= disco_fused_conv_bwd_weight_workspace_bytes,
    256-byte aligned), then a tcgen05 GEMM over the pixels (reduction split
    across CTAs into fp32 partials, summed in a fixed order: deterministic).
-   Takes bf16 with the tensor-core forward shape (W_in % 8 == 0, W_in >= 64,
+   Takes bf16 or fp16 with the tensor-core forward shape (W_in % 8 == 0, W_in >= 64,
    s in {1, 2}, K <= 9), H_out*W_out, Cin*K and Cout multiples of 8,
    Cin*K >= 64 and Cout >= 16; else DISCO_ERR_UNSUPPORTED.  Asynchronous on
    `stream`. */
