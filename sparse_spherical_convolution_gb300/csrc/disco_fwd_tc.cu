@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (bc < a.BC && wo < a.Wout) {
               __nv_bfloat16* dst = a.X + (((size_t)bc * K + k) * a.Hout + ho) * a.Wout + wo;
               const int n = min(16, a.Wout - wo);
-              if (n == 16) {
+              // 16-byte stores need 16-byte aligned rows: W_out % 8 == 0 (wo is a multiple of 16)
+              if (n == 16 && (a.Wout & 7) == 0) {
                 uint32_t w32[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {

@@ -37,6 +37,8 @@ SMALL = [
     ((16, 32, 2), (16, 32, 2), 1, 3, 3 * math.pi / 16, 1, 5, torch.float32),      # Legendre-Gauss
     ((40, 128, 2), (40, 64, 2), 1, 3, 3 * math.pi / 40, 2, 70, torch.bfloat16),   # Legendre-Gauss, s = 2, tensor cores
     ((65, 256, 1), (32, 128, 2), 1, 3, 3 * math.pi / 32, 1, 130, torch.bfloat16), # poles -> Legendre-Gauss
+    ((24, 72, 0), (12, 36, 0), 1, 3, 3 * math.pi / 12, 2, 20, torch.bfloat16),    # W_out % 8 != 0: non-persistent forward tiles
+    ((24, 72, 0), (12, 36, 0), 1, 3, 3 * math.pi / 12, 1, 9, torch.float16),      # the same in fp16
 ]
 
 

@@ -36,6 +36,7 @@ SMALL = [
     ((16, 36, 0), (16, 36, 0), 1, 3, 2 * math.pi / 16, 1, 16, 40),        # W_in % 8 != 0: on-chip path
     ((32, 64, 0), (16, 32, 0), 1, 3, 3 * math.pi / 16, 1, 24, 8),         # Cin % 16 != 0 (workspace path)
     ((33, 64, 1), (33, 64, 1), 1, 3, 3 * math.pi / 32, 2, 64, 48),        # TMA GEMMs: ragged pixel tile, 3 dX n-tiles
+    ((24, 72, 0), (12, 36, 0), 1, 3, 3 * math.pi / 12, 1, 32, 24),        # X from the non-persistent forward tiles
 ]
 
 
