@@ -39,6 +39,9 @@ SMALL = [
     ((65, 256, 1), (32, 128, 2), 1, 3, 3 * math.pi / 32, 1, 130, torch.bfloat16), # poles -> Legendre-Gauss
     ((24, 72, 0), (12, 36, 0), 1, 3, 3 * math.pi / 12, 2, 20, torch.bfloat16),    # W_out % 8 != 0: non-persistent forward tiles
     ((24, 72, 0), (12, 36, 0), 1, 3, 3 * math.pi / 12, 1, 9, torch.float16),      # the same in fp16
+    ((2, 8, 0), (2, 8, 0), 0, 1, 2.5, 1, 3, torch.float32),                        # 2 rows, cutoff near the whole sphere
+    ((3, 16, 1), (3, 16, 1), 1, 2, 2.0, 1, 4, torch.bfloat16),                    # 3-row pole grid (zero-weight poles)
+    ((2, 8, 2), (2, 8, 2), 1, 1, 2.5, 2, 2, torch.float32),                        # 2-row Legendre-Gauss grid
 ]
 
 

@@ -20,6 +20,8 @@ CASES = [(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff) for w in WORKLOADS.va
     ((16, 31, 0), (16, 31, 0), 0, 2, 2 * math.pi / 16),    # odd ring width
     ((8, 16, 2), (8, 16, 2), 0, 3, 2 * math.pi / 8),       # Legendre-Gauss grids
     ((33, 64, 1), (16, 32, 2), 1, 3, 3 * math.pi / 16),    # pole grid -> Legendre-Gauss, s = 2
+    ((3, 16, 1), (3, 16, 1), 1, 2, 2.0),                   # 3-row pole grid, one input-row group
+    ((2, 8, 2), (2, 8, 2), 1, 1, 2.5),                     # 2-row Legendre-Gauss grid, full rings
 ] + [(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff) for w in PAGE_WORKLOADS.values()]
 
 
