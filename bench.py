@@ -426,7 +426,7 @@ def run_reference(args):
     for _ in range(args.steps):
         cb = cpu_baseline(w, args.cpu_budget_s, ref)
         vals.append(cb["value"])
-    v = statistics.median(vals)
+    v = round(statistics.median(vals), 4)
     out = {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
