@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   disco_grp_ent* infos = reinterpret_cast<disco_grp_ent*>(smem + kStages * Cfg::kStageBytes);
   uint8_t* outbuf = smem + kStages * Cfg::kStageBytes + Cfg::kInfoBytes;  // [2] gx pieces for TMA stores
   uint64_t* bars = reinterpret_cast<uint64_t*>(outbuf + 2 * Cfg::kOutBytes);
-  uint64_t* fullA = bars;                         // [kStages] G boxes + psi block landed
+  uint64_t* fullA = bars;                         // [kStages] G boxes landed
   uint64_t* fullB = bars + kStages;               // [kStages] T built (192 arrivals)
   uint64_t* empty = bars + 2 * kStages;           // [kStages] MMAs of the stage done (commit)
   uint64_t* info_full = bars + 3 * kStages;       // [2] entry list landed
@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* info_cnt = reinterpret_cast<int32_t*>(bars + 3 * kStages + 7);  // [2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kStages + 8);
   volatile int* tile_id = reinterpret_cast<volatile int*>(bars + 3 * kStages + 9);  // [2], -1 = no more tiles
+  // [kStages] psi block landed: the builders start T while the G boxes are still in flight
+  uint64_t* fullT = bars + 3 * kStages + 10;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = a.ntx * a.nty * a.ntz;
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&fullA[s], 1);
+      mbar_init(&fullT[s], 1);
       mbar_init(&fullB[s], kBuilderThreads);
       mbar_init(&empty[s], 1);
     }
@@ -214,9 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
     const int nsteps = min(4, (int)en.KB - 4 * c);
     const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
-    mbar_expect_tx(&fullA[s], nbox * kBoxBytes + Cfg::kTabBytes);
+    mbar_expect_tx(&fullT[s], Cfg::kTabBytes);
     bulk_copy(st + 2 * kBoxBytes + kTBytes, a.gtab + en.off + (size_t)(k * en.nch + c) * grp_block(S),
-              Cfg::kTabBytes, &fullA[s]);
+              Cfg::kTabBytes, &fullT[s]);
+    mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
     const int row = k * a.Hout + en.ho;
     for (int bb = 0; bb < nbox; ++bb) {
       const int col0 = qb - en.MW + 64 * (c + bb);
@@ -234,7 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // exits (n = one past its last issued item)
   auto drain_own = [&](int n, int who) {
     for (int li = n - 1; li >= 0 && li >= n - 2 * kStages; --li)
-      if ((li & 1) == who) mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
+      if ((li & 1) == who) {
+        mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
+        mbar_wait(&fullT[li % kStages], (li / kStages) & 1, kWaitLimit);
+      }
   };
 
   if (warp == 0) {
@@ -377,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < a.K && ok; ++k)
           for (int c = 0; c < nch; ++c, ++i) {
             const int s = i % kStages;
-            // fullA(i) is issued only after the MMAs of the stage's previous item completed
-            const bool mine = mbar_wait(&fullA[s], (i / kStages) & 1, kWaitLimit) && !*abort_flag;
+            // the stage's copies are issued only after the MMAs of its previous item
+            // completed; T needs only the psi block
+            const bool mine = mbar_wait(&fullT[s], (i / kStages) & 1, kWaitLimit) && !*abort_flag;
             ok = all_named(mine, 1, kBuilderThreads);
             if (!ok) break;
             uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
