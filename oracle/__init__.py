@@ -9,7 +9,9 @@ Pinned by the ``not gpu`` tests (dense brute force with independent vector
 geometry, adjoint identity, longitude equivariance, the indicator-basis
 neighbourhood sum, normalisation and symmetry invariants, hand-derived closed
 forms, numpy einsum; the weight gradient against numpy einsum, the adjoint
-identity with the einsum and the linearity of the fused forward in W).
+identity with the einsum and the linearity of the fused forward in W; the
+error scale S = sum |terms| returned beside every output against |M| of the
+independent dense matrix and numpy einsum of absolute values).
 """
 from __future__ import annotations
 

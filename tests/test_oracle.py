@@ -10,7 +10,10 @@
   neighbourhood sum: pins the neighbourhood rule;
 * hand-derived closed forms on a 2x4 grid (tests/golden/closed_form_2x4.txt);
 * hat partition of unity, constant-field normalisation, psi symmetries;
-* the einsum against numpy.einsum (a textbook contraction).
+* the einsum against numpy.einsum (a textbook contraction);
+* the error scale S = sum |terms| of every output (the denominator of every
+  parity bar) against |M| of the dense brute force and numpy.einsum of
+  absolute values, with planted mistakes (S summed over k, |W| dropped).
 """
 import math
 import os
@@ -417,3 +420,108 @@ def test_planted_mistakes_are_caught():
     bad = np.array(X)
     bad[:, :, 2::3] *= -1
     assert np.abs(bad - ref).max() > 1e-3
+
+
+# ------------------------------------------------------------------ error scale
+#
+# Every parity bar divides by S = sum over the elementary terms of |term|.  The
+# oracle returns S beside each output; these tests recompute it from the
+# independent vector-geometry dense matrix M (|psi| is |M| entry by entry) and
+# from numpy.einsum, so that an S inflated or deflated anywhere (summed over k,
+# a dropped |W| factor, the wrong transpose) fails here.
+
+def _rel(a, b):
+    return float(np.max(np.abs(a - b) / np.maximum(np.abs(b), 1e-300)))
+
+
+@pytest.mark.parametrize("case", TINY, ids=lambda c: f"{c[0]}->{c[1]}-k{c[2]}r{c[3]}")
+def test_error_scale_of_the_contractions(case):
+    gi, go, kind, nrad, cut = case
+    psi = oracle.build_psi(gi, go, kind, nrad, cut)
+    Ma = np.abs(_vector_dense(gi, go, kind, nrad, cut))     # [K*Hout*Wout, Hin*Win]
+    rng = np.random.default_rng(8)
+    B, C = 2, 2
+    x = rng.standard_normal((B, C, gi[0], gi[1]))
+    G = rng.standard_normal((B, C, psi.K, go[0], go[1]))
+    _, SX = oracle.fwd(psi, x)
+    ref = (Ma @ np.abs(x).reshape(B * C, -1).T).T.reshape(SX.shape)
+    assert _rel(SX, ref) < 1e-12
+    _, Sg = oracle.bwd(psi, G)
+    ref = (Ma.T @ np.abs(G).reshape(B * C, -1).T).T.reshape(Sg.shape)
+    assert _rel(Sg, ref) < 1e-12
+
+
+@pytest.mark.parametrize("case", TINY[:5], ids=lambda c: f"{c[0]}->{c[1]}")
+def test_error_scale_of_the_einsums_and_fused_paths(case):
+    gi, go, kind, nrad, cut = case
+    psi = oracle.build_psi(gi, go, kind, nrad, cut)
+    K = psi.K
+    Ma = np.abs(_vector_dense(gi, go, kind, nrad, cut))
+    rng = np.random.default_rng(9)
+    B, Cin, Cout = 2, 3, 4
+    x = rng.standard_normal((B, Cin, gi[0], gi[1]))
+    W = rng.standard_normal((Cout, Cin, K))
+    dy = rng.standard_normal((B, Cout, go[0], go[1]))
+    # einsum adjoint: SdX = sum_o |W[o,c,k]| |dy[b,o,p]|
+    _, SdX = oracle.einsum_t(W, dy)
+    ref_dX = np.einsum("ock,bohw->bckhw", np.abs(W), np.abs(dy))
+    assert _rel(SdX, ref_dX) < 1e-12
+    # fused forward: S = sum_{c,k} |W| sum_n |psi x| = einsum(|W|, |M| |x|)
+    _, Sy = oracle.fused(psi, x, W)
+    SX = (Ma @ np.abs(x).reshape(B * Cin, -1).T).T.reshape(B, Cin, K, go[0], go[1])
+    ref_y = np.einsum("ock,bckhw->bohw", np.abs(W), SX)
+    assert _rel(Sy, ref_y) < 1e-12
+    # fused input gradient: S = |M|^T applied to sum_o |W| |dy|
+    _, Sgx = oracle.fused_bwd_input(psi, dy, W)
+    ref_gx = (Ma.T @ ref_dX.reshape(B * Cin, -1).T).T.reshape(Sgx.shape)
+    assert _rel(Sgx, ref_gx) < 1e-12
+    # weight gradient: S = sum_{b,p} |dy| (|M| |x|)
+    _, SdW = oracle.fused_bwd_weight(psi, x, dy)
+    ref_w = np.einsum("bohw,bckhw->ock", np.abs(dy), SX)
+    assert _rel(SdW, ref_w) < 1e-12
+    # the sampled-point forms return the same S at their points
+    n = 40
+    p4 = np.stack([rng.integers(0, B * Cin, n), rng.integers(0, K, n),
+                   rng.integers(0, go[0], n), rng.integers(0, go[1], n)], 1)
+    _, s = oracle.fwd_points(psi, x.astype(np.float32), p4)
+    x32 = np.abs(x.astype(np.float32).astype(np.float64))
+    SX32 = (Ma @ x32.reshape(B * Cin, -1).T).T.reshape(B * Cin, K, go[0], go[1])
+    assert _rel(s, SX32[tuple(p4.T)]) < 1e-12
+    py = np.stack([rng.integers(0, B, n), rng.integers(0, Cout, n),
+                   rng.integers(0, go[0], n), rng.integers(0, go[1], n)], 1)
+    _, s = oracle.fused_points(psi, x.astype(np.float32), W.astype(np.float32), py)
+    W32 = np.abs(W.astype(np.float32).astype(np.float64))
+    ref = np.einsum("ock,bckhw->bohw", W32, SX32.reshape(B, Cin, K, go[0], go[1]))
+    assert _rel(s, ref[tuple(py.T)]) < 1e-12
+    G = rng.standard_normal((B, Cin, K, go[0], go[1])).astype(np.float32)
+    p3 = np.stack([rng.integers(0, B * Cin, n), rng.integers(0, gi[0], n), rng.integers(0, gi[1], n)], 1)
+    _, s = oracle.bwd_points(psi, G, p3)
+    ref = (Ma.T @ np.abs(G.astype(np.float64)).reshape(B * Cin, -1).T).T.reshape(B * Cin, gi[0], gi[1])
+    assert _rel(s, ref[tuple(p3.T)]) < 1e-12
+    pg = np.stack([rng.integers(0, B, n), rng.integers(0, Cin, n),
+                   rng.integers(0, gi[0], n), rng.integers(0, gi[1], n)], 1)
+    _, s = oracle.fused_bwd_points(psi, dy.astype(np.float32), W.astype(np.float32), pg)
+    d32 = np.abs(dy.astype(np.float32).astype(np.float64))
+    dX32 = np.einsum("ock,bohw->bckhw", W32, d32)
+    ref = (Ma.T @ dX32.reshape(B * Cin, -1).T).T.reshape(B, Cin, gi[0], gi[1])
+    assert _rel(s, ref[tuple(pg.T)]) < 1e-12
+
+
+def test_error_scale_planted_mistakes_are_caught():
+    """An S off by a factor (summed over k, or with |W| dropped) fails the pins."""
+    gi, go, kind, nrad, cut = TINY[2]
+    psi = oracle.build_psi(gi, go, kind, nrad, cut)
+    Ma = np.abs(_vector_dense(gi, go, kind, nrad, cut))
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((1, 2, gi[0], gi[1]))
+    _, SX = oracle.fwd(psi, x)
+    ref = (Ma @ np.abs(x).reshape(2, -1).T).T.reshape(SX.shape)
+    summed_over_k = np.repeat(SX.sum(axis=2, keepdims=True), psi.K, axis=2)
+    assert _rel(summed_over_k, ref) > 1e-3
+    assert _rel(SX * psi.K, ref) > 1e-3
+    W = rng.standard_normal((3, 2, psi.K))
+    dy = rng.standard_normal((1, 3, go[0], go[1]))
+    _, SdX = oracle.einsum_t(W, dy)
+    no_w = np.einsum("ock,bohw->bckhw", np.ones_like(W), np.abs(dy))
+    assert _rel(no_w, np.einsum("ock,bohw->bckhw", np.abs(W), np.abs(dy))) > 1e-3
+    assert _rel(SdX, np.einsum("ock,bohw->bckhw", np.abs(W), np.abs(dy))) < 1e-12
