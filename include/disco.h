@@ -2,13 +2,14 @@
  * disco.h -- C ABI of the GB300 (sm_103a) DISCO convolution library.
  *
  * DISCO = discrete-continuous convolution on the sphere.  The operations
- * follow the DISCO Kernel Development Guide (torch-harmonics), whose
- * §Architecture snapshot lists the three kernels this library provides:
- *   forward   "CSR sparse contraction inp -> (B,C,K,H,W)"
- *   backward  "CSR transpose contraction (B,C,K,H,W) -> inp"
- *   fused     "contraction + einsum"  (y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo])
- * and whose §kpacked layout describes the neighbour-list form of psi built
- * once at init ("converts CSR psi to kpacked layout at init time").
+ * follow the DISCO Kernel Development Guide (torch-harmonics).  Its
+ * §Architecture snapshot names three kernels, all provided here:
+ *   forward   the sparse contraction of the input grid into X[B,C,K,H,W]
+ *   backward  its transpose, from X-shaped gradients back to the input grid
+ *   fused     the contraction followed by the channel/basis einsum
+ *             (y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo])
+ * Its §kpacked layout describes the neighbour-list form of psi, with the
+ * values of all K basis functions side by side, built once at init.
  *
  * Conventions (all entry points):
  *  - Every tensor argument is a DEVICE pointer to a dense, C-contiguous array
@@ -52,10 +53,10 @@ typedef enum {
   DISCO_ERR_WORKSPACE = -7           /* workspace missing or too small */
 } disco_status;
 
-/* Element type of the activations (x, X, G, gx, y, dy) and of W.  fp16 is
-   the page's third precision (§benchmark: "all 3 precisions (fp32, bf16,
-   fp16)"); it runs the same kernels as bf16 with fp16 operands (and fp16
-   copies of the Toeplitz tables), fp32 accumulation. */
+/* Element type of the activations (x, X, G, gx, y, dy) and of W.  The
+   guide's §Profiling / Serial Benchmarks section names fp32, bf16 and fp16
+   as the precisions to cover; fp16 runs the same kernels as bf16 with fp16
+   operands (and fp16 copies of the Toeplitz tables), fp32 accumulation. */
 typedef enum { DISCO_F32 = 0, DISCO_BF16 = 1, DISCO_F16 = 2 } disco_dtype;
 
 /* Latitude rows of a grid.  poles = 0 (equiangular, midpoints): colatitude
@@ -220,7 +221,7 @@ DISCO_API int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes
 DISCO_API int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, float* pack_val,
                                        int64_t* pack_count, int32_t nbr_pad, void* stream);
 
-/* Forward S2 contraction (§Architecture snapshot "forward"; §Backward
+/* Forward S2 contraction (§Architecture snapshot, forward kernel; §Backward
    direction: gather, each output pixel reads a bounded neighbourhood):
      X[b,c,k,ho,wo] = sum_{(hi,wi) in row (k,ho)} psi[k,ho,hi,wi]
                         * x[b,c,hi,(wi + wo*s) mod W_in]
@@ -232,7 +233,7 @@ DISCO_API int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, 
 DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
-/* Transpose contraction (§Architecture snapshot "backward"; §Backward
+/* Transpose contraction (§Architecture snapshot, backward kernel; §Backward
    direction: gather direction, each input pixel accumulates from its
    neighbourhood, no atomics):  gx = psi^T G, i.e.
      gx[b,c,hi,wi] = sum_{k,ho,wo} sum_{wi0: (wi0 + wo*s) mod W_in = wi}
@@ -253,8 +254,9 @@ DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B
 DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
                                                   disco_dtype dtype);
 
-/* Fused convolution (§Architecture snapshot "_disco_s2_fused_conv_optimized:
-   contraction + einsum"):  y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo]
+/* Fused convolution (§Architecture snapshot: the fused kernel, the
+   contraction followed by the einsum):
+     y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo]
    with X the forward contraction, in one call:
      - where the tensor-core contraction takes the shape, X is produced by it
        into `workspace` (disco_fused_conv_workspace_bytes bytes) and the
@@ -278,7 +280,11 @@ DISCO_API int disco_fused_conv(const disco_psi* psi, const void* x, const void* 
 DISCO_API size_t disco_fused_conv_bwd_input_workspace_bytes(const disco_psi* psi, int32_t B,
                                                   int32_t Cin, disco_dtype dtype);
 
-/* Input gradient of the fused convolution:
+/* Input gradient of the fused convolution (§Architecture snapshot: the
+   fused kernel and its backward are paired through an autograd function;
+   §Backward direction for the transpose).  The guide gives no formula; the
+   plain reading is the gradient of y = einsum(W, psi x) with respect to x,
+   the upstream gradient routed through W^T first, then the transpose:
      dX[b,c,k,ho,wo] = sum_o W[o,c,k] dy[b,o,ho,wo]   (tcgen05 tensor cores)
      gx = psi^T dX                                    (the transpose contraction)
    dy: [B, Cout, H_out, W_out], W: [Cout, Cin, K], gx: [B, Cin, H_in, W_in],
@@ -375,7 +381,9 @@ DISCO_API int disco_bwd_host(const disco_psi* psi, const void* G_host, void* gx_
    input-row group reading more output rows than it can hold, bit 4 = the
    wait of disco_check_wait_timeout ran out; a kernel that times out stops
    issuing work, frees its tensor memory and returns, leaving its outputs
-   incomplete).  clear != 0 resets the word. */
+   incomplete).  clear != 0 resets the word and frees every slot of the tile
+   schedulers (see disco_check_sched_hold): call it with clear != 0 only
+   while no other thread launches work of this library on the device. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
 
 /* Diagnostic of the failure path, asynchronous: launches one small kernel
@@ -386,6 +394,19 @@ DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
    usable.  Lets a test check that a timed-out wait reaches
    disco_device_status. */
 DISCO_API int disco_check_wait_timeout(uint32_t limit, void* stream);
+
+/* Diagnostic of the recovery path of the tile schedulers, synchronous.  The
+   persistent tensor-core kernels take their tiles from a counter in one of
+   1024 slots of a library-owned device table (slot = launch number mod
+   1024); a launch waits, bounded, while an earlier launch still holds its
+   slot.  This call marks the slot that the next launch will take as held by
+   a launch that never finishes, as a launch that failed part-way could leave
+   it.  The next persistent launch then gives up after its bounded wait
+   (about 3-7 s), computes nothing and sets bit 2 (forward) or bit 3
+   (transpose) of the status word; disco_device_status with clear != 0 frees
+   every slot again.  Lets a test check that a held slot is recovered; no
+   kernel faults, traps or hangs. */
+DISCO_API int disco_check_sched_hold(void);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ __all__ = [
     "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
-    "disco_fused_conv_bwd_weight", "disco_device_status", "library_path",
+    "disco_fused_conv_bwd_weight", "disco_device_status", "disco_check_sched_hold", "library_path",
     "load_library", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = [
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
     "disco_fused_conv_bwd_weight", "disco_device_status", "disco_psi_export_kpacked",
     "disco_check_wait_timeout", "disco_host_workspace_bytes", "disco_fwd_host", "disco_bwd_host",
+    "disco_check_sched_hold",
 ]
 
 
@@ -110,6 +111,8 @@ def load_library():
         getattr(lib, nm).argtypes = [PP, P, P, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_check_wait_timeout.restype = ctypes.c_int
     lib.disco_check_wait_timeout.argtypes = [ctypes.c_uint32, P]
+    lib.disco_check_sched_hold.restype = ctypes.c_int
+    lib.disco_check_sched_hold.argtypes = []
     lib.disco_psi_export_kpacked.restype = ctypes.c_int
     lib.disco_psi_export_kpacked.argtypes = [PP, P, P, P, I32, P]
     lib.disco_fwd.restype = ctypes.c_int
@@ -169,6 +172,50 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _dev(t, name: str, numel: int, dtype=None):
+    """Pointer of a device tensor after checking it: on the current CUDA
+    device, contiguous, `numel` elements, and of `dtype` when given.  A
+    mismatch raises DiscoError(-1) before any call into the library."""
+    import torch
+    if t is None:
+        raise DiscoError(-1, f"{name} is None")
+    if not t.is_cuda or t.device.index != torch.cuda.current_device():
+        raise DiscoError(-1, f"{name} must be a tensor on the current CUDA device, got {t.device}")
+    if dtype is not None and t.dtype != dtype:
+        raise DiscoError(-1, f"{name} has dtype {t.dtype}, the call's dtype is {dtype}")
+    if t.numel() != int(numel):
+        raise DiscoError(-1, f"{name} has {t.numel()} elements, the call needs {int(numel)}")
+    return _ptr(t)
+
+
+def _host(t, name: str, numel: int, dtype=None):
+    """Pointer of a host (CPU) tensor after the same checks as _dev."""
+    if t is None or t.is_cuda:
+        raise DiscoError(-1, f"{name} must be a CPU tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise DiscoError(-1, f"{name} has dtype {t.dtype}, the call's dtype is {dtype}")
+    if t.numel() != int(numel):
+        raise DiscoError(-1, f"{name} has {t.numel()} elements, the call needs {int(numel)}")
+    return _ptr(t)
+
+
+def _ws(t, name: str = "workspace"):
+    """(pointer, bytes) of an optional device workspace."""
+    import torch
+    if t is None:
+        return None, 0
+    if not t.is_cuda or t.device.index != torch.cuda.current_device():
+        raise DiscoError(-1, f"{name} must be a tensor on the current CUDA device")
+    return _ptr(t), t.numel() * t.element_size()
+
+
+def _sizes(psi):
+    """(H_in*W_in, K*H_out*W_out, H_out*W_out, K) of a built psi."""
+    pin = psi.grid_in.nlat * psi.grid_in.nlon
+    pout = psi.grid_out.nlat * psi.grid_out.nlon
+    return pin, psi.K * pout, pout, psi.K
+
+
 # ------------------------------------------------------------------ ABI calls
 
 def disco_version() -> int:
@@ -201,15 +248,13 @@ def disco_psi_plan(grid_in, grid_out, basis, workspace, stream=None) -> disco_ps
     psi = disco_psi()
     _check(load_library().disco_psi_plan(
         ctypes.byref(_grid(grid_in)), ctypes.byref(_grid(grid_out)), ctypes.byref(basis),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
-        ctypes.byref(psi)))
+        *_ws(workspace), _stream(stream), ctypes.byref(psi)))
     return psi
 
 
 def disco_build_psi_kpacked(psi: disco_psi, buffer, workspace, stream=None) -> None:
     _check(load_library().disco_build_psi_kpacked(
-        ctypes.byref(psi), _ptr(buffer), buffer.numel() * buffer.element_size(), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        ctypes.byref(psi), *_ws(buffer, "buffer"), *_ws(workspace), _stream(stream)))
 
 
 def disco_host_workspace_bytes(psi: disco_psi, B: int, C: int, forward: bool, dtype=DISCO_BF16) -> int:
@@ -218,15 +263,23 @@ def disco_host_workspace_bytes(psi: disco_psi, B: int, C: int, forward: bool, dt
 
 def disco_fwd_host(psi: disco_psi, x_host, X_host, B: int, C: int, workspace, stream=None) -> None:
     """x_host, X_host: CPU tensors (pinned for overlap); workspace: device."""
-    _check(load_library().disco_fwd_host(ctypes.byref(psi), _ptr(x_host), _ptr(X_host), B, C, _dtype(x_host),
-                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+    pin, pX, _, _ = _sizes(psi)
+    dt = x_host.dtype
+    xp = _host(x_host, "x_host", B * C * pin, dt)
+    Xp = _host(X_host, "X_host", B * C * pX, dt)
+    wp, wn = _ws(workspace)
+    _check(load_library().disco_fwd_host(ctypes.byref(psi), xp, Xp, B, C, _dtype(x_host), wp, wn,
                                          _stream(stream)))
 
 
 def disco_bwd_host(psi: disco_psi, G_host, gx_host, B: int, C: int, workspace, stream=None) -> None:
     """G_host, gx_host: CPU tensors (pinned for overlap); workspace: device."""
-    _check(load_library().disco_bwd_host(ctypes.byref(psi), _ptr(G_host), _ptr(gx_host), B, C, _dtype(G_host),
-                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+    pin, pX, _, _ = _sizes(psi)
+    dt = G_host.dtype
+    Gp = _host(G_host, "G_host", B * C * pX, dt)
+    gp = _host(gx_host, "gx_host", B * C * pin, dt)
+    wp, wn = _ws(workspace)
+    _check(load_library().disco_bwd_host(ctypes.byref(psi), Gp, gp, B, C, _dtype(G_host), wp, wn,
                                          _stream(stream)))
 
 
@@ -234,20 +287,33 @@ def disco_check_wait_timeout(limit: int, stream=None) -> None:
     _check(load_library().disco_check_wait_timeout(limit, _stream(stream)))
 
 
+def disco_check_sched_hold() -> None:
+    """Marks the next persistent launch's scheduler slot as held (diagnostic)."""
+    _check(load_library().disco_check_sched_hold())
+
+
 def disco_psi_export_kpacked(psi: disco_psi, pack_idx, pack_val, pack_count, nbr_pad: int,
                              stream=None) -> None:
-    _check(load_library().disco_psi_export_kpacked(ctypes.byref(psi), _ptr(pack_idx), _ptr(pack_val),
-                                                   _ptr(pack_count), nbr_pad, _stream(stream)))
+    import torch
+    H = psi.grid_out.nlat
+    ip = _dev(pack_idx, "pack_idx", H * nbr_pad * 2, torch.int64)
+    vp = _dev(pack_val, "pack_val", H * nbr_pad * psi.K_pad, torch.float32)
+    cp = _dev(pack_count, "pack_count", H, torch.int64)
+    _check(load_library().disco_psi_export_kpacked(ctypes.byref(psi), ip, vp, cp, nbr_pad, _stream(stream)))
 
 
 def disco_fwd(psi: disco_psi, x, X, B: int, C: int, stream=None) -> None:
-    _check(load_library().disco_fwd(ctypes.byref(psi), _ptr(x), _ptr(X), B, C, _dtype(x),
-                                    _stream(stream)))
+    pin, pX, _, _ = _sizes(psi)
+    xp = _dev(x, "x", B * C * pin)
+    Xp = _dev(X, "X", B * C * pX, x.dtype)
+    _check(load_library().disco_fwd(ctypes.byref(psi), xp, Xp, B, C, _dtype(x), _stream(stream)))
 
 
 def disco_bwd(psi: disco_psi, G, gx, B: int, C: int, stream=None) -> None:
-    _check(load_library().disco_bwd(ctypes.byref(psi), _ptr(G), _ptr(gx), B, C, _dtype(G),
-                                    _stream(stream)))
+    pin, pX, _, _ = _sizes(psi)
+    Gp = _dev(G, "G", B * C * pX)
+    gp = _dev(gx, "gx", B * C * pin, G.dtype)
+    _check(load_library().disco_bwd(ctypes.byref(psi), Gp, gp, B, C, _dtype(G), _stream(stream)))
 
 
 def disco_fused_conv_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:
@@ -256,9 +322,13 @@ def disco_fused_conv_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DIS
 
 def disco_fused_conv(psi: disco_psi, x, W, y, B: int, Cin: int, Cout: int, workspace=None,
                      stream=None) -> None:
-    nws = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(load_library().disco_fused_conv(ctypes.byref(psi), _ptr(x), _ptr(W), _ptr(y), B, Cin,
-                                           Cout, _dtype(x), _ptr(workspace), nws, _stream(stream)))
+    pin, _, pout, K = _sizes(psi)
+    xp = _dev(x, "x", B * Cin * pin)
+    Wp = _dev(W, "W", Cout * Cin * K, x.dtype)
+    yp = _dev(y, "y", B * Cout * pout, x.dtype)
+    wp, wn = _ws(workspace)
+    _check(load_library().disco_fused_conv(ctypes.byref(psi), xp, Wp, yp, B, Cin, Cout, _dtype(x), wp, wn,
+                                           _stream(stream)))
 
 
 def disco_fused_conv_bwd_input_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:
@@ -267,10 +337,13 @@ def disco_fused_conv_bwd_input_workspace_bytes(psi: disco_psi, B: int, Cin: int,
 
 def disco_fused_conv_bwd_input(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout: int,
                                workspace, stream=None) -> None:
-    _check(load_library().disco_fused_conv_bwd_input(
-        ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy),
-        _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
-        _stream(stream)))
+    pin, _, pout, K = _sizes(psi)
+    dp = _dev(dy, "dy", B * Cout * pout)
+    Wp = _dev(W, "W", Cout * Cin * K, dy.dtype)
+    gp = _dev(gx, "gx", B * Cin * pin, dy.dtype)
+    wp, wn = _ws(workspace)
+    _check(load_library().disco_fused_conv_bwd_input(ctypes.byref(psi), dp, Wp, gp, B, Cin, Cout, _dtype(dy),
+                                                     wp, wn, _stream(stream)))
 
 
 def disco_fused_conv_bwd_weight_workspace_bytes(psi: disco_psi, B: int, Cin: int, Cout: int,
@@ -280,18 +353,25 @@ def disco_fused_conv_bwd_weight_workspace_bytes(psi: disco_psi, B: int, Cin: int
 
 def disco_fused_conv_bwd_weight(psi: disco_psi, x, dy, dW, B: int, Cin: int, Cout: int,
                                 workspace, stream=None) -> None:
-    _check(load_library().disco_fused_conv_bwd_weight(
-        ctypes.byref(psi), _ptr(x), _ptr(dy), _ptr(dW), B, Cin, Cout, _dtype(x),
-        _ptr(workspace), workspace.numel() * workspace.element_size() if workspace is not None else 0,
-        _stream(stream)))
+    pin, _, pout, K = _sizes(psi)
+    xp = _dev(x, "x", B * Cin * pin)
+    dp = _dev(dy, "dy", B * Cout * pout, x.dtype)
+    Wp = _dev(dW, "dW", Cout * Cin * K, x.dtype)
+    wp, wn = _ws(workspace)
+    _check(load_library().disco_fused_conv_bwd_weight(ctypes.byref(psi), xp, dp, Wp, B, Cin, Cout, _dtype(x),
+                                                      wp, wn, _stream(stream)))
 
 
 def disco_fused_conv_bwd_input_noalloc(psi: disco_psi, dy, W, gx, B: int, Cin: int, Cout: int,
                                        stream=None) -> None:
     """disco_fused_conv_bwd_input without a workspace argument: the library's
     fixed device scratch holds dX (see include/disco.h for limits and rules)."""
+    pin, _, pout, K = _sizes(psi)
+    dp = _dev(dy, "dy", B * Cout * pout)
+    Wp = _dev(W, "W", Cout * Cin * K, dy.dtype)
+    gp = _dev(gx, "gx", B * Cin * pin, dy.dtype)
     _check(load_library().disco_fused_conv_bwd_input_noalloc(
-        ctypes.byref(psi), _ptr(dy), _ptr(W), _ptr(gx), B, Cin, Cout, _dtype(dy), _stream(stream)))
+        ctypes.byref(psi), dp, Wp, gp, B, Cin, Cout, _dtype(dy), _stream(stream)))
 
 
 def disco_device_status(clear: bool = True) -> int:

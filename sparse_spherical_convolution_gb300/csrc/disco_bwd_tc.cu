@@ -1,7 +1,8 @@
 // disco_bwd_tc.cu -- the transpose DISCO contraction on the tensor cores (bf16).
 //
 // DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
-// ("backward: CSR transpose contraction (B,C,K,H,W) -> inp") and §Backward
+// (the backward kernel: the transpose of the sparse contraction, from
+// X-shaped gradients back to the input grid) and §Backward
 // direction (gather direction, each input pixel accumulates from its
 // neighbourhood, no atomics; every output element has exactly one owner).
 //
@@ -621,6 +622,22 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
 }
 
 }  // namespace
+
+// Marks the slot of launch `id` as held by a launch that never finishes, as a
+// slot left behind by a failed launch would be (diagnostic of the recovery
+// path; the next launch's claims then run out and flag the status word).
+cudaError_t btc_sched_hold(unsigned long long id) {
+  SchedSlot s{~0ull, 0, 0};
+  return cudaMemcpyToSymbol(g_btc_sched, &s, sizeof(SchedSlot), (id % kSchedSlots) * sizeof(SchedSlot));
+}
+
+// Frees every slot.  Only while no kernel of this library runs on the device
+// (disco_device_status calls it after synchronising the device): a slot that
+// a failed launch left held is then usable again.
+cudaError_t btc_sched_reset() {
+  static const SchedSlot zero[kSchedSlots] = {};
+  return cudaMemcpyToSymbol(g_btc_sched, zero, sizeof(zero));
+}
 
 cudaError_t btc_status(int32_t* v, bool clear) {
   int32_t t = 0;

@@ -2,6 +2,7 @@
 
 #include <stdarg.h>
 #include <atomic>
+#include <mutex>
 #include <stdio.h>
 
 #include "disco_internal.cuh"
@@ -42,9 +43,46 @@ int check_device() {
   return DISCO_OK;
 }
 
-unsigned long long next_launch_id() {
-  static std::atomic<unsigned long long> seq{0};
-  return seq.fetch_add(1, std::memory_order_relaxed) + 1;
+namespace {
+std::atomic<unsigned long long> g_launch_seq{0};
+}
+
+unsigned long long next_launch_id() { return g_launch_seq.fetch_add(1, std::memory_order_relaxed) + 1; }
+
+unsigned long long peek_launch_id() { return g_launch_seq.load(std::memory_order_relaxed) + 1; }
+
+int check_dev_ptr(const void* p, const char* name) {
+  if (!p) return fail(DISCO_ERR_INVALID_ARG, "%s is null", name);
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // the failed query is not a sticky error; clear it
+    return fail(DISCO_ERR_INVALID_ARG, "%s: the CUDA runtime does not know this pointer (%s)", name,
+                cudaGetErrorString(e));
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+    return fail(DISCO_ERR_INVALID_ARG, "%s is not device memory (host or unregistered pointer)", name);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(DISCO_ERR_CUDA, "cudaGetDevice failed");
+  if (at.type == cudaMemoryTypeDevice && at.device != dev)
+    return fail(DISCO_ERR_INVALID_ARG, "%s lives on device %d, the current device is %d", name, at.device, dev);
+  return DISCO_OK;
+}
+
+void* current_context() {
+  using GetCtx = int (*)(void**);
+  static GetCtx fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCtx>(p);
+  });
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
 }
 
 int check_launch(const char* what) {

@@ -340,13 +340,17 @@ int dispatch(bool fwd, int kind, int K, const ContractArgs& a, cudaStream_t st) 
   return fail(DISCO_ERR_UNSUPPORTED, "K = %d (kind %d) has no contraction kernel", K, kind);
 }
 
+}  // namespace
+
 int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t B, int32_t C,
-             disco_dtype dtype, void* stream) {
+             disco_dtype dtype, void* stream, bool check_ptrs) {
   int st = check_psi(psi);
   if (st) return st;
   if ((st = check_device())) return st;
   if (!in || !out) return fail(DISCO_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(in) || !aligned16(out)) return fail(DISCO_ERR_ALIGNMENT, "tensors must be 16-byte aligned");
+  if (check_ptrs && ((st = check_dev_ptr(in, fwd ? "x" : "G")) || (st = check_dev_ptr(out, fwd ? "X" : "gx"))))
+    return st;
   if (B < 1 || C < 1) return fail(DISCO_ERR_INVALID_ARG, "B and C must be >= 1");
   if ((int64_t)B * C > (int64_t)65535 * 32) return fail(DISCO_ERR_UNSUPPORTED, "B*C too large");
   if (dtype != DISCO_F32 && dtype != DISCO_BF16 && dtype != DISCO_F16) return fail(DISCO_ERR_UNSUPPORTED, "dtype");
@@ -387,15 +391,14 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
                      : dispatch<__nv_bfloat16, 2>(fwd, kind, K, a, s);
 }
 
-}  // namespace
 }  // namespace disco
 
 extern "C" int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
                          disco_dtype dtype, void* stream) {
-  return disco::contract(true, psi, x, X, B, C, dtype, stream);
+  return disco::contract(true, psi, x, X, B, C, dtype, stream, true);
 }
 
 extern "C" int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
                          disco_dtype dtype, void* stream) {
-  return disco::contract(false, psi, G, gx, B, C, dtype, stream);
+  return disco::contract(false, psi, G, gx, B, C, dtype, stream, true);
 }

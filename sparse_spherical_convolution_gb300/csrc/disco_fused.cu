@@ -1,8 +1,8 @@
 // disco_fused.cu -- fused DISCO convolution and its input gradient on the
 // sm_100-family tensor cores (tcgen05 MMA, fp32 accumulators in TMEM).
 //
-// DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot:
-// "_disco_s2_fused_conv_optimized: custom_op: contraction + einsum".  The
+// DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
+// (the fused kernel: the contraction followed by the einsum).  The
 // einsum y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo] is a dense
 // contraction over C*K, so it runs on the tensor cores; the contraction that
 // produces X stays the CUDA-core gather of disco_fwd and X never reaches
@@ -598,6 +598,8 @@ int check_fused_common(const disco_psi* psi, const void* a, const void* W, const
   if (!a || !W || !out) return fail(DISCO_ERR_INVALID_ARG, "null tensor pointer");
   if (!aligned16(a) || !aligned16(W) || !aligned16(out))
     return fail(DISCO_ERR_ALIGNMENT, "tensors must be 16-byte aligned");
+  if ((st = check_dev_ptr(a, "input")) || (st = check_dev_ptr(W, "W")) || (st = check_dev_ptr(out, "output")))
+    return st;
   if (dtype != DISCO_BF16 && dtype != DISCO_F16) return fail(DISCO_ERR_UNSUPPORTED, "fused paths take bf16 or fp16");
   if (B < 1 || Cin < 1 || Cout < 1) return fail(DISCO_ERR_INVALID_ARG, "B, Cin, Cout must be >= 1");
   if (B > 65535) return fail(DISCO_ERR_UNSUPPORTED, "B > 65535");
@@ -659,6 +661,7 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
     if (!workspace || workspace_bytes < need)
       return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     if (!aligned16(workspace)) return fail(DISCO_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    if ((st = check_dev_ptr(workspace, "workspace"))) return st;
     return fused_tc(psi, x, W, y, B, Cin, Cout, workspace, s, dtype == DISCO_F16);
   }
   if (dtype == DISCO_F16)
@@ -694,6 +697,11 @@ extern "C" size_t disco_fused_conv_bwd_input_workspace_bytes(const disco_psi* ps
   return (size_t)B * Cin * psi->K * psi->grid_out.nlat * psi->grid_out.nlon * 2;
 }
 
+// The input gradient with dX in `workspace`; the caller has checked the
+// arguments and the workspace (a caller buffer or the library's own scratch).
+static int fused_bwd_input(const disco_psi* psi, const void* dy, const void* W, void* gx, int32_t B,
+                           int32_t Cin, int32_t Cout, disco_dtype dtype, void* workspace, void* stream);
+
 extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, const void* W,
                                           void* gx, int32_t B, int32_t Cin, int32_t Cout,
                                           disco_dtype dtype, void* workspace,
@@ -704,6 +712,13 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
   if (!workspace || workspace_bytes < need)
     return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
   if (!aligned16(workspace)) return fail(DISCO_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  if ((st = check_dev_ptr(workspace, "workspace"))) return st;
+  return fused_bwd_input(psi, dy, W, gx, B, Cin, Cout, dtype, workspace, stream);
+}
+
+static int fused_bwd_input(const disco_psi* psi, const void* dy, const void* W, void* gx, int32_t B,
+                           int32_t Cin, int32_t Cout, disco_dtype dtype, void* workspace, void* stream) {
+  int st = DISCO_OK;
   GemmArgs g;
   g.dy = (const __nv_bfloat16*)dy;
   g.W = (const __nv_bfloat16*)W;
@@ -737,7 +752,7 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
     st = check_launch("dX gemm");
   }
   if (st) return st;
-  return disco_bwd(psi, workspace, gx, B, Cin, dtype, stream);
+  return contract(false, psi, workspace, gx, B, Cin, dtype, stream, false);
 }
 
 static size_t align256z(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -766,6 +781,7 @@ extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, 
   if (!workspace || workspace_bytes < need) return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(DISCO_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if ((st = check_dev_ptr(workspace, "workspace"))) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
   const int CK = Cin * psi->K;
@@ -808,7 +824,21 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
   if (e == cudaSuccess) e = tc_status(flags, clear != 0);
   if (e == cudaSuccess) e = btc_status(flags, clear != 0);
   if (e == cudaSuccess) e = gemm_status(flags, clear != 0);
+  // a launch that failed may have left its scheduler slot held; with the
+  // device synchronised no kernel of this library runs, so every slot is free
+  if (e == cudaSuccess && clear) e = fwd_sched_reset();
+  if (e == cudaSuccess && clear) e = btc_sched_reset();
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
+  return DISCO_OK;
+}
+
+extern "C" int disco_check_sched_hold(void) {
+  int st = check_device();
+  if (st) return st;
+  const unsigned long long id = peek_launch_id();
+  cudaError_t e = fwd_sched_hold(id);
+  if (e == cudaSuccess) e = btc_sched_hold(id);
+  if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "scheduler slot: %s", cudaGetErrorString(e));
   return DISCO_OK;
 }
 
@@ -833,7 +863,12 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+// per device: the context the address was looked up in, and the address
+struct NoAllocAddr {
+  void* ctx = nullptr;
+  void* ptr = nullptr;
+};
+NoAllocAddr g_noalloc[kMaxDevices];
 
 int noalloc_scratch(void** out) {
   int dev = 0;
@@ -841,14 +876,19 @@ int noalloc_scratch(void** out) {
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(DISCO_ERR_UNSUPPORTED, "device index %d >= %d", dev, kMaxDevices);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocAddr& c = g_noalloc[dev];
+  void* ctx = current_context();
+  // the cached address holds only for the context it was taken in: after a
+  // device reset the array lives at a new address of a new context
+  if (!c.ptr || !ctx || ctx != c.ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || !p)
       return fail(DISCO_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = p;
+    c.ptr = p;
+    c.ctx = current_context();  // the lookup made the device's context current
   }
-  *out = g_noalloc_ptr[dev];
+  *out = c.ptr;
   return DISCO_OK;
 }
 
@@ -870,6 +910,5 @@ extern "C" int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const vo
   if ((st = noalloc_scratch(&scratch))) return st;
   // dX is fully rewritten by the GEMM before the transpose reads it, so
   // nothing left in the scratch by an earlier call needs clearing.
-  return disco_fused_conv_bwd_input(psi, dy, W, gx, B, Cin, Cout, dtype, scratch,
-                                    kNoAllocScratchBytes, stream);
+  return fused_bwd_input(psi, dy, W, gx, B, Cin, Cout, dtype, scratch, stream);
 }

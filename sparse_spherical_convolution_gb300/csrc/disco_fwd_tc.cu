@@ -1,7 +1,8 @@
 // disco_fwd_tc.cu -- the forward DISCO contraction on the tensor cores (bf16).
 //
 // DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
-// ("forward: CSR sparse contraction inp -> (B,C,K,H,W)") and §kpacked layout
+// (the forward kernel: the sparse contraction of the input grid into
+// X[B,C,K,H,W]) and §kpacked layout
 // (psi values of all K side by side, which is what lets a tensor-core tile
 // produce all basis functions at once; the page's WGMMA kernel is the Hopper
 // form of the same idea).
@@ -943,6 +944,22 @@ bool fits_tc(const disco_psi* psi) {
 }
 
 }  // namespace
+
+// Marks the slot of launch `id` as held by a launch that never finishes, as a
+// slot left behind by a failed launch would be (diagnostic of the recovery
+// path; the next launch's claims then run out and flag the status word).
+cudaError_t fwd_sched_hold(unsigned long long id) {
+  SchedSlot s{~0ull, 0, 0};
+  return cudaMemcpyToSymbol(g_fwd_sched, &s, sizeof(SchedSlot), (id % kSchedSlots) * sizeof(SchedSlot));
+}
+
+// Frees every slot.  Only while no kernel of this library runs on the device
+// (disco_device_status calls it after synchronising the device): a slot that
+// a failed launch left held is then usable again.
+cudaError_t fwd_sched_reset() {
+  static const SchedSlot zero[kSchedSlots] = {};
+  return cudaMemcpyToSymbol(g_fwd_sched, zero, sizeof(zero));
+}
 
 // Reads (and optionally clears) this unit's status word; the caller has
 // synchronised the device.

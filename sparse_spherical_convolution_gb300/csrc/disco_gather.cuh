@@ -9,8 +9,8 @@
 //               (x[hi, S (wo_blk + o0 + t) + delta]  +/-  x[hi, S (wo_blk + o0 + t) - delta])
 //
 // (minus for the sin component of an anisotropic basis).  This is the CSR
-// gather of the DISCO Kernel Development Guide, §Backward direction ("each
-// output pixel reads from a bounded neighbourhood"), walked run by run with
+// gather of the DISCO Kernel Development Guide, §Backward direction (every
+// output pixel reads only its own bounded neighbourhood), walked run by run with
 // mirrored offsets paired.  The NT threads of the group stage the wrapped
 // window of the current run in shared memory (fp32, row pitch = 1 mod 32)
 // and the pair weights next to it; the group synchronises on named barrier

@@ -3,7 +3,7 @@
 // its input gradient.
 //
 // DISCO Kernel Development Guide (torch-harmonics), §Architecture snapshot
-// ("_disco_s2_fused_conv_optimized: contraction + einsum"): after the S2
+// (the fused kernel: the contraction followed by an einsum): after the S2
 // contraction, y[b,o,ho,wo] = sum_{c,k} W[o,c,k] X[b,c,k,ho,wo].  Both GEMMs
 // here have the form
 //

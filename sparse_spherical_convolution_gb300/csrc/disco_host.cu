@@ -26,6 +26,7 @@ constexpr int kMaxDevices = 64;
 
 struct CopyStreams {
   cudaStream_t in = nullptr, out = nullptr;
+  void* ctx = nullptr;  // the context the streams belong to
 };
 std::mutex g_copy_mu;
 CopyStreams g_copy[kMaxDevices];
@@ -36,10 +37,21 @@ int copy_streams(CopyStreams* cs) {
     return fail(DISCO_ERR_CUDA, "no current device for the copy streams");
   std::lock_guard<std::mutex> lock(g_copy_mu);
   CopyStreams& c = g_copy[dev];
-  if (!c.in) {
+  void* ctx = current_context();
+  if (!ctx) {  // no context current on this thread yet: let the runtime make it current
+    (void)cudaStreamQuery(nullptr);
+    ctx = current_context();
+  }
+  // streams of a context that was reset are gone with it: make new ones (the
+  // old handles are not destroyed, they no longer name anything)
+  if (!c.in || (ctx && ctx != c.ctx)) {
+    c.in = c.out = nullptr;
     if (cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess)
+        cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) != cudaSuccess) {
+      c.in = c.out = nullptr;
       return fail(DISCO_ERR_CUDA, "copy stream creation failed");
+    }
+    c.ctx = current_context();
   }
   *cs = c;
   return DISCO_OK;
@@ -79,6 +91,7 @@ int contract_host(bool fwd, const disco_psi* psi, const void* in_host, void* out
   if (!workspace || workspace_bytes < need) return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(DISCO_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if ((rc = check_dev_ptr(workspace, "workspace"))) return rc;
   CopyStreams cs;
   if ((rc = copy_streams(&cs))) return rc;
   int64_t ip, op;

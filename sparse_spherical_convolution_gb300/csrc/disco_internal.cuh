@@ -23,11 +23,36 @@ int check_launch(const char* what);
 // Process-unique, nonzero id of a kernel launch (selects the launch's
 // scheduler slot, disco_sched.cuh); thread-safe.
 unsigned long long next_launch_id();
+// The id the next launch will get (without taking it).
+unsigned long long peek_launch_id();
+
+// DISCO_OK if `p` is device (or managed) memory of the current device, else
+// DISCO_ERR_INVALID_ARG naming `name`: a host pointer or a pointer of another
+// device is refused on the host instead of faulting in a kernel.
+int check_dev_ptr(const void* p, const char* name);
+
+// The calling thread's current CUDA context (driver handle), or null.  Caches
+// of device addresses and library streams are keyed on it as well as on the
+// device index, so a context that was reset and re-created is seen as new.
+void* current_context();
+
+// Scheduler tables of the persistent kernels (disco_sched.cuh): mark the slot
+// of launch `id` as held by a launch that never finishes (a diagnostic), or
+// free every slot (only while no kernel of this library runs on the device).
+cudaError_t fwd_sched_hold(unsigned long long id);
+cudaError_t fwd_sched_reset();
+cudaError_t btc_sched_hold(unsigned long long id);
+cudaError_t btc_sched_reset();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Validates the pieces of psi every hot call relies on.
 int check_psi(const disco_psi* psi);
+
+// disco_fwd (fwd) / disco_bwd (!fwd); check_ptrs = false skips the device-
+// pointer queries, for buffers the library itself hands in.
+int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t B, int32_t C,
+             disco_dtype dtype, void* stream, bool check_ptrs);
 
 // Forward contraction on the tensor cores (bf16); DISCO_ERR_UNSUPPORTED,
 // without launching, for shapes that path does not take.

@@ -732,6 +732,7 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
     return fail(DISCO_ERR_WORKSPACE, "psi workspace needs %zu bytes", need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(DISCO_ERR_ALIGNMENT, "psi workspace must be 256-byte aligned");
+  if ((st = check_dev_ptr(workspace, "psi workspace"))) return st;
   Workspace ws;
   carve_workspace(g, (char*)workspace, &ws);
   g.lg = ws.lg;
@@ -817,6 +818,7 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
   size_t need = carve_workspace(g, nullptr, nullptr);
   if (!workspace || workspace_bytes < need)
     return fail(DISCO_ERR_WORKSPACE, "psi workspace needs %zu bytes", need);
+  if ((st = check_dev_ptr(buffer, "psi buffer")) || (st = check_dev_ptr(workspace, "psi workspace"))) return st;
   Workspace ws;
   carve_workspace(g, (char*)workspace, &ws);
   g.lg = ws.lg;  // Legendre-Gauss tables left in the workspace by disco_psi_plan
@@ -884,6 +886,9 @@ extern "C" int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx,
     return fail(DISCO_ERR_ALIGNMENT, "outputs must be aligned to their element size");
   if (nbr_pad < 1 || nbr_pad < psi->max_row)
     return fail(DISCO_ERR_INVALID_ARG, "nbr_pad (%d) must be >= max_row (%d)", nbr_pad, psi->max_row);
+  if ((st = check_dev_ptr(pack_idx, "pack_idx")) || (st = check_dev_ptr(pack_val, "pack_val")) ||
+      (st = check_dev_ptr(pack_count, "pack_count")))
+    return st;
   export_kpacked_kernel<<<psi->grid_out.nlat, 256, 0, (cudaStream_t)stream>>>(
       psi->row_ptr, psi->idx, psi->val, psi->K_pad, nbr_pad, pack_idx, pack_val, pack_count);
   return check_launch("psi kpacked export");

@@ -73,3 +73,21 @@ def test_hot_calls_reject_unbuilt_psi_before_any_launch(lib):
     assert so.disco_fused_conv(ctypes.byref(empty), None, None, None, 1, 16, 16, 1, None, 0, None) == -1
     assert so.disco_fused_conv_bwd_input(ctypes.byref(empty), None, None, None, 1, 16, 16, 1,
                                          None, 0, None) == -1
+
+
+def test_binding_rejects_host_tensors_before_the_library(lib):
+    """The binding checks device, dtype and size in Python first: a CPU tensor
+    never reaches a kernel (this runs without a GPU)."""
+    import torch
+    psi = lib.disco_psi()
+    psi.grid_in = lib.disco_grid(8, 16, 0)
+    psi.grid_out = lib.disco_grid(8, 16, 0)
+    psi.K = 3
+    x = torch.zeros((1, 2, 8, 16), dtype=torch.float32)
+    X = torch.zeros((1, 2, 3, 8, 16), dtype=torch.float32)
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_fwd(psi, x, X, 1, 2)
+    assert e.value.status == -1 and "CUDA device" in str(e.value)
+    with pytest.raises(lib.DiscoError) as e:
+        lib.disco_fwd_host(psi, x, X[:, :1], 1, 2, None)
+    assert e.value.status == -1 and "elements" in str(e.value)

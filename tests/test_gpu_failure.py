@@ -47,3 +47,43 @@ def test_wait_check_rejects_bad_limits(lib):
         with pytest.raises(lib.DiscoError) as e:
             lib.disco_check_wait_timeout(bad)
         assert e.value.status == -1
+
+
+def _held_slot_case(lib, fwd: bool):
+    """A scheduler slot left held (as a launch that failed part-way could
+    leave it): the next persistent launch gives up after its bounded wait,
+    computes nothing and flags the status word; clearing the status frees the
+    slot and the launch after that is correct."""
+    gi = go = (64, 128, 0)
+    ref = oracle.build_psi(gi, go, 0, 5, 3 * math.pi / 64)
+    psi = lib.Psi(gi, go, 0, 5, 3 * math.pi / 64)
+    g = torch.Generator().manual_seed(43)
+    B, C = 1, 130
+    x = torch.randn((B, C, 64, 128), generator=g).to(torch.bfloat16).cuda()
+    G = torch.randn((B, C, ref.K, 64, 128), generator=g).to(torch.bfloat16).cuda()
+    inp, shape = (x, (B, C, ref.K, 64, 128)) if fwd else (G, (B, C, 64, 128))
+    call = lib.disco_fwd if fwd else lib.disco_bwd
+    bit = 4 if fwd else 8
+    assert lib.disco_device_status(clear=True) == 0
+    out = torch.full(shape, 3.0, dtype=torch.bfloat16, device="cuda")
+    lib.disco_check_sched_hold()
+    call(psi.c, inp, out, B, C)
+    assert lib.disco_device_status(clear=False) & bit
+    assert torch.all(out == 3.0)            # no tile was taken
+    assert lib.disco_device_status(clear=True) & bit   # read, then cleared: the slot is free again
+    out.fill_(3.0)
+    call(psi.c, inp, out, B, C)
+    assert lib.disco_device_status() == 0
+    if fwd:
+        want, S = oracle.fwd(ref, to_np32(x))
+    else:
+        want, S = oracle.bwd(ref, to_np32(G))
+    assert rel_err(to_np32(out), want, S) <= TOL[torch.bfloat16]
+
+
+def test_held_scheduler_slot_is_recovered_forward(lib):
+    _held_slot_case(lib, True)
+
+
+def test_held_scheduler_slot_is_recovered_transpose(lib):
+    _held_slot_case(lib, False)

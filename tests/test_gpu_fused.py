@@ -159,7 +159,7 @@ def test_fused_rejects_unsupported(lib):
         lib.disco_fused_conv(psi.c, x, W, y, 1, 8, 8)  # no workspace for the tensor-core path
     assert e.value.status == -7
     with pytest.raises(lib.DiscoError) as e:
-        lib.disco_fused_conv(psi.c, x.float(), W, y, 1, 8, 8)  # fp32
+        lib.disco_fused_conv(psi.c, x.float(), W.float(), y.float(), 1, 8, 8)  # fp32
     assert e.value.status == -2
     psi36 = lib.Psi((16, 36, 0), (16, 36, 0), 0, 3, 2 * math.pi / 16)  # on-chip path
     x36 = torch.zeros((1, 8, 16, 36), dtype=BF, device="cuda")

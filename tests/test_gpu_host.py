@@ -73,3 +73,29 @@ def test_host_workspace_rule(lib):
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_fwd_host(psi.c, x, X, 1, 4, small)
     assert e.value.status == -7
+
+
+def test_binding_rejects_wrong_device_dtype_and_size(lib):
+    """The binding refuses host tensors, mixed dtypes and wrong element counts
+    before calling the library; the C ABI itself refuses host pointers."""
+    import ctypes
+    psi = lib.Psi((64, 128, 0), (64, 128, 0), 0, 5, 3 * math.pi / 64)
+    K = psi.c.K
+    x = torch.zeros((1, 4, 64, 128), dtype=torch.bfloat16, device="cuda")
+    X = torch.full((1, 4, K, 64, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    for bad_x, bad_X in [(x.cpu(), X), (x, X.float()), (x, X[:, :3]), (x[:, :3], X)]:
+        with pytest.raises(lib.DiscoError) as e:
+            lib.disco_fwd(psi.c, bad_x.contiguous(), bad_X.contiguous(), 1, 4)
+        assert e.value.status == -1
+    W = torch.zeros((8, 4, K), dtype=torch.float16, device="cuda")
+    y = torch.zeros((1, 8, 64, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.DiscoError):
+        lib.disco_fused_conv(psi.c, x, W, y, 1, 4, 8)      # W of another dtype
+    # through the C ABI: a host buffer as X is refused on the host
+    so = lib.load_library()
+    host = (ctypes.c_uint16 * X.numel())()
+    st = so.disco_fwd(ctypes.byref(psi.c), ctypes.c_void_p(x.data_ptr()), ctypes.cast(host, ctypes.c_void_p),
+                      1, 4, lib.DISCO_BF16, None)
+    assert st == -1 and "device memory" in lib.disco_last_error()
+    torch.cuda.synchronize()
+    assert torch.all(X == 5.0)

@@ -5,9 +5,10 @@ memory themselves (a runtime whose allocator owns all device memory, or a hot
 loop that must not risk cudaMalloc's implicit device synchronisation).  It
 keeps dX in the library's fixed device scratch instead of a caller workspace.
 This file is collected last on purpose: it checks, through the C ABI, that
-the variant matches the workspace entry point within the suite's tolerance on
-two calls in a row (the scratch keeps the previous call's contents), and
-that oversized problems are rejected before any launch.  It needs nothing
+the variant gives bit for bit the workspace entry point's result on two calls
+in a row (the scratch keeps the previous call's contents; bf16 and fp16),
+that the first call is within the suite's bar of the fp64 oracle, and that
+oversized problems are rejected before any launch.  It needs nothing
 from the other test files, so it also passes alone in a fresh process.
 """
 import math
@@ -32,32 +33,39 @@ def lib():
 
 
 CASES = [
-    # (grid_in, grid_out, kind, nrad, cutoff, B, Cin, Cout)
-    ((64, 128, 0), (64, 128, 0), 0, 5, 3 * math.pi / 64, 2, 32, 48),
-    ((128, 256, 0), (64, 128, 0), 1, 3, 3 * math.pi / 64, 1, 32, 64),
+    # (grid_in, grid_out, kind, nrad, cutoff, B, Cin, Cout, dtype)
+    ((64, 128, 0), (64, 128, 0), 0, 5, 3 * math.pi / 64, 2, 32, 48, BF),     # CUDA-core dX GEMM
+    ((128, 256, 0), (64, 128, 0), 1, 3, 3 * math.pi / 64, 1, 32, 64, BF),    # tensor-core dX GEMM + transpose
+    ((128, 256, 0), (64, 128, 0), 1, 3, 3 * math.pi / 64, 1, 64, 64, torch.float16),  # fp16: Cin*K % 64 == 0
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}->{c[1]}")
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}->{c[1]}-{str(c[8])[6:]}")
 def test_noalloc_matches_workspace_entry_point_twice(lib, case):
-    gi, go, kind, nrad, cut, B, Cin, Cout = case
+    gi, go, kind, nrad, cut, B, Cin, Cout, dt = case
     psi = lib.Psi(gi, go, kind, nrad, cut)
     K = psi.c.K
     g = torch.Generator().manual_seed(21)
-    W = (torch.randn((Cout, Cin, K), generator=g) / math.sqrt(Cin * K)).to(BF).cuda()
+    W = (torch.randn((Cout, Cin, K), generator=g) / math.sqrt(Cin * K)).to(dt).cuda()
     ref = oracle.build_psi(gi, go, kind, nrad, cut)
-    ws = torch.empty(lib.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, Cin),
+    ws = torch.empty(lib.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, Cin, _CODE[dt]),
                      dtype=torch.uint8, device="cuda")
     for call in range(2):  # two calls in a row with different inputs
-        dy = torch.randn((B, Cout, go[0], go[1]), generator=g).to(BF).cuda()
-        want = torch.empty((B, Cin, gi[0], gi[1]), dtype=BF, device="cuda")
-        got = torch.full((B, Cin, gi[0], gi[1]), float("nan"), dtype=BF, device="cuda")
+        dy = torch.randn((B, Cout, go[0], go[1]), generator=g).to(dt).cuda()
+        want = torch.empty((B, Cin, gi[0], gi[1]), dtype=dt, device="cuda")
+        got = torch.full((B, Cin, gi[0], gi[1]), float("nan"), dtype=dt, device="cuda")
         lib.disco_fused_conv_bwd_input(psi.c, dy, W, want, B, Cin, Cout, ws)
         lib.disco_fused_conv_bwd_input_noalloc(psi.c, dy, W, got, B, Cin, Cout)
         torch.cuda.synchronize()
-        assert not torch.isnan(got).any()
-        _, S = oracle.fused_bwd_input(ref, to_np32(dy), to_np32(W))
-        assert rel_err(to_np32(got), to_np32(want), S) <= TOL[BF], call
+        assert lib.disco_device_status() == 0
+        # the same kernels on the same inputs: bit for bit the workspace result
+        assert torch.equal(got, want), call
+        if call == 0:  # and within the suite's bar of the fp64 oracle
+            gxo, S = oracle.fused_bwd_input(ref, to_np32(dy), to_np32(W))
+            assert rel_err(to_np32(got), gxo, S) <= TOL[dt]
+
+
+_CODE = {BF: 1, torch.float16: 2}
 
 
 def test_noalloc_rejects_problems_beyond_the_fixed_scratch(lib):
