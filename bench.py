@@ -165,7 +165,7 @@ def run_ours(args):
     y = torch.empty(sh["y"], dtype=dt, device=dev)
     gx2 = torch.empty(sh["x"], dtype=dt, device=dev)
     wsb = max(d.disco_fused_conv_bwd_input_workspace_bytes(psi.c, B, C),
-              d.disco_fused_conv_workspace_bytes(psi.c, B, C))
+              d.disco_fused_conv_workspace_bytes(psi.c, B, C, Co))
     wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)  # shared: the calls run in sequence
     stream = torch.cuda.current_stream(dev)
     alg = algorithmic(w, psi.c)
@@ -322,10 +322,39 @@ def run_ours(args):
     # launch each, so their events time the kernel alone.  Bound: HBM, with
     # the algorithmic bytes of one launch (input + output + psi).
     dom = "bwd" if med["bwd"] >= med["fwd"] else "fwd"
-    dom_kernel = {"bwd": "bwd_tc_kernel", "fwd": "fwd_tcp_kernel"}[dom]
+    kname = {"bwd": "bwd_tc_kernel", "fwd": "fwd_tcp_kernel"}
+    dom_kernel = kname[dom]
     dom_bytes = alg[dom + "_bytes"]
     achieved = dom_bytes / (med[dom] * 1e-3) / 1e9
     traffic = _traffic_from_profiles(dom_kernel, w.name)
+    other = "fwd" if dom == "bwd" else "bwd"
+    o_ach = alg[other + "_bytes"] / (med[other] * 1e-3) / 1e9
+
+    def hbm_frac(nbytes, ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4), "ms": round(ms, 3)}
+
+    # the fused calls against their own compulsory bytes, and the einsum's
+    # tensor rate inside the fused call (its flops over the whole call's time:
+    # a lower bound on the einsum's own rate) against the sustained bf16 peak
+    tc_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    fused_calls = None
+    if "fused_bytes" in alg:
+        ein_tf = alg["einsum_flops"] / (med["fused"] * 1e-3) / 1e12
+        # the fused call is the forward kernel (X into the workspace) followed by
+        # the einsum GEMM, so the GEMM's own time is the call's minus the forward's
+        ein_ms = med["fused"] - med["fwd"]
+        fused_calls = {
+            "einsum_gemm": {"ms_by_subtraction": round(ein_ms, 3),
+                            "tflops": round(alg["einsum_flops"] / (ein_ms * 1e-3) / 1e12, 1) if ein_ms > 0 else None,
+                            "frac_of_sustained_peak": round(alg["einsum_flops"] / (ein_ms * 1e-3) / 1e12 / tc_peak, 4)
+                            if ein_ms > 0 else None},
+            "fused_conv": hbm_frac(alg["fused_bytes"], med["fused"]),
+            "fused_conv_bwd_input": hbm_frac(alg["fused_bwd_bytes"], med["fused_bwd"]),
+            "einsum": {"flops_per_call": alg["einsum_flops"], "tflops_over_fused_call": round(ein_tf, 1),
+                       "peak_tflops": tc_peak, "frac_of_sustained_peak": round(ein_tf / tc_peak, 4),
+                       "peak_source": f"{peak_src} (cuBLAS bf16, sustained)"},
+        }
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
@@ -347,6 +376,12 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "ms_per_launch": round(med[dom], 3),
                      "peak_source": f"{peak_src} (copy bandwidth)"},
+        "roofline_other_contraction": {"bound": "hbm", "kernel": kname[other], "achieved": round(o_ach, 1),
+                                       "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": round(o_ach / peaks["hbm_gbs"], 4),
+                                       "algorithmic_bytes_per_launch": alg[other + "_bytes"],
+                                       "ms_per_launch": round(med[other], 3)},
+        "fused_calls": fused_calls,
         "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peak_src,
         "clocks": clocks, "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
     }
@@ -441,7 +476,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)

@@ -247,11 +247,11 @@ DISCO_API int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B,
 DISCO_API int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
               disco_dtype dtype, void* stream);
 
-/* Device workspace bytes of disco_fused_conv: the intermediate
-   X[B, Cin, K, H_out, W_out] (dtype) when the tensor-core contraction takes
-   the shape (bf16 or fp16, W_in % 8 == 0, W_in >= 64, s in {1, 2}, K <= 9),
-   else 0 (no workspace needed). */
-DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
+/* Device workspace bytes of disco_fused_conv for these B, Cin, Cout: the
+   intermediate X[B, Cin, K, H_out, W_out] (dtype) when the tensor-core
+   contraction takes the shape (bf16 or fp16, W_in % 8 == 0, W_in >= 64,
+   s in {1, 2}, K <= 9), else 0 (no workspace needed). */
+DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin, int32_t Cout,
                                                   disco_dtype dtype);
 
 /* Fused convolution (§Architecture snapshot: the fused kernel, the
@@ -267,10 +267,11 @@ DISCO_API size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t 
        Cin % 16 == 0).
    Accumulation is fp32 (TMEM); X is rounded to the dtype before the einsum.
    x: [B, Cin, H_in, W_in], W: [Cout, Cin, K], y: [B, Cout, H_out, W_out],
-   all bf16 or all fp16 (dtype); Cout <= 256.  fp16 needs the tensor-core
-   path: the forward shape above and the GEMM shape (H_out*W_out, Cin*K and
-   Cout multiples of 8, Cin*K >= 64, Cout >= 16); else DISCO_ERR_UNSUPPORTED
-   before any launch. */
+   all bf16 or all fp16 (dtype).  The einsum GEMM takes any Cout (tiles of
+   up to 256 outputs); the CUDA-core gather path needs Cout <= 256.  fp16
+   needs the tensor-core path: the forward shape above and the GEMM shape
+   (H_out*W_out, Cin*K and Cout multiples of 8, Cin*K >= 64, Cout >= 16);
+   else DISCO_ERR_UNSUPPORTED before any launch. */
 DISCO_API int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
                      int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
                      void* workspace, size_t workspace_bytes, void* stream);

@@ -8,9 +8,9 @@
  * header, table or constant with the CUDA path.
  *
  * What it computes (DISCO Kernel Development Guide, torch-harmonics,
- * §Architecture snapshot: "CSR sparse contraction inp -> (B,C,K,H,W)" and
- * "CSR transpose contraction (B,C,K,H,W) -> inp"; §kpacked layout for the
- * neighbour-list form).  The page names the operations but does not give the
+ * §Architecture snapshot: the sparse contraction of the input grid into
+ * X[B,C,K,H,W] and its transpose back to the input grid; §kpacked layout for
+ * the neighbour-list form).  The page names the operations but does not give the
  * basis, quadrature or normalisation; the definitions below are the plainest
  * readings of the workload text and every one of them is listed with its
  * reason in the design notes:

@@ -120,7 +120,7 @@ def load_library():
     lib.disco_bwd.restype = ctypes.c_int
     lib.disco_bwd.argtypes = [PP, P, P, I32, I32, ctypes.c_int, P]
     lib.disco_fused_conv_workspace_bytes.restype = SZ
-    lib.disco_fused_conv_workspace_bytes.argtypes = [PP, I32, I32, ctypes.c_int]
+    lib.disco_fused_conv_workspace_bytes.argtypes = [PP, I32, I32, I32, ctypes.c_int]
     lib.disco_fused_conv.restype = ctypes.c_int
     lib.disco_fused_conv.argtypes = [PP, P, P, P, I32, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_fused_conv_bwd_input_workspace_bytes.restype = SZ
@@ -316,8 +316,8 @@ def disco_bwd(psi: disco_psi, G, gx, B: int, C: int, stream=None) -> None:
     _check(load_library().disco_bwd(ctypes.byref(psi), Gp, gp, B, C, _dtype(G), _stream(stream)))
 
 
-def disco_fused_conv_workspace_bytes(psi: disco_psi, B: int, Cin: int, dtype=DISCO_BF16) -> int:
-    return load_library().disco_fused_conv_workspace_bytes(ctypes.byref(psi), B, Cin, dtype)
+def disco_fused_conv_workspace_bytes(psi: disco_psi, B: int, Cin: int, Cout: int, dtype=DISCO_BF16) -> int:
+    return load_library().disco_fused_conv_workspace_bytes(ctypes.byref(psi), B, Cin, Cout, dtype)
 
 
 def disco_fused_conv(psi: disco_psi, x, W, y, B: int, Cin: int, Cout: int, workspace=None,

@@ -395,10 +395,12 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
 
 extern "C" int disco_fwd(const disco_psi* psi, const void* x, void* X, int32_t B, int32_t C,
                          disco_dtype dtype, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fwd");
   return disco::contract(true, psi, x, X, B, C, dtype, stream, true);
 }
 
 extern "C" int disco_bwd(const disco_psi* psi, const void* G, void* gx, int32_t B, int32_t C,
                          disco_dtype dtype, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_bwd");
   return disco::contract(false, psi, G, gx, B, C, dtype, stream, true);
 }

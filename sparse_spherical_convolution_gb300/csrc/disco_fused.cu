@@ -618,9 +618,9 @@ using namespace disco;
 static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y, int32_t B, int32_t Cin,
                     int32_t Cout, void* X, cudaStream_t s, bool f16) {
   const int64_t P = (int64_t)psi->grid_out.nlat * psi->grid_out.nlon;
-  if (f16 && !(gemm_tc_supported(P, Cin * psi->K, Cout) && Cout <= 256))
+  if (f16 && !gemm_tc_supported(P, Cin * psi->K, Cout))
     return fail(DISCO_ERR_UNSUPPORTED, "fp16 fused conv: needs the tensor-core einsum shape "
-                "(H_out*W_out, Cin*K, Cout multiples of 8, Cin*K >= 64, 16 <= Cout <= 256)");
+                "(H_out*W_out, Cin*K, Cout multiples of 8, Cin*K >= 64, Cout >= 16)");
   int st = fwd_tensor_core(psi, x, X, B * Cin, s, f16);
   if (st) return st;
   st = einsum_tensor_core(X, W, y, B, Cin * psi->K, Cout, P, s, f16);
@@ -642,9 +642,10 @@ static int fused_tc(const disco_psi* psi, const void* x, const void* W, void* y,
   return check_launch("einsum");
 }
 
-extern "C" size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin,
+extern "C" size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t B, int32_t Cin, int32_t Cout,
                                                    disco_dtype dtype) {
-  if (!psi || B < 1 || Cin < 1 || (dtype != DISCO_BF16 && dtype != DISCO_F16) || !fwd_tc_supported(psi, B * Cin))
+  if (!psi || B < 1 || Cin < 1 || Cout < 1 || (dtype != DISCO_BF16 && dtype != DISCO_F16) ||
+      !fwd_tc_supported(psi, B * Cin))
     return 0;
   return (size_t)B * Cin * psi->K * psi->grid_out.nlat * psi->grid_out.nlon * 2;
 }
@@ -652,11 +653,11 @@ extern "C" size_t disco_fused_conv_workspace_bytes(const disco_psi* psi, int32_t
 extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void* W, void* y,
                                 int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
                                 void* workspace, size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fused_conv");
   int st = check_fused_common(psi, x, W, y, B, Cin, Cout, dtype);
   if (st) return st;
-  if (Cout > 256) return fail(DISCO_ERR_UNSUPPORTED, "Cout must be <= 256");
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t need = disco_fused_conv_workspace_bytes(psi, B, Cin, dtype);
+  const size_t need = disco_fused_conv_workspace_bytes(psi, B, Cin, Cout, dtype);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
       return fail(DISCO_ERR_WORKSPACE, "workspace needs %zu bytes", need);
@@ -669,6 +670,7 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
                 "W_in >= 64, K <= 9)");
   // shapes the tensor-core contraction does not take: X built on chip by the
   // CUDA-core gather, einsum on the tensor cores
+  if (Cout > 256) return fail(DISCO_ERR_UNSUPPORTED, "Cout must be <= 256 on the CUDA-core gather path");
   if (Cin % kFCC != 0) return fail(DISCO_ERR_UNSUPPORTED, "Cin must be a multiple of %d", kFCC);
   FusedArgs a;
   a.x = (const __nv_bfloat16*)x;
@@ -706,6 +708,7 @@ extern "C" int disco_fused_conv_bwd_input(const disco_psi* psi, const void* dy, 
                                           void* gx, int32_t B, int32_t Cin, int32_t Cout,
                                           disco_dtype dtype, void* workspace,
                                           size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fused_conv_bwd_input");
   int st = check_fused_common(psi, dy, W, gx, B, Cin, Cout, dtype);
   if (st) return st;
   size_t need = disco_fused_conv_bwd_input_workspace_bytes(psi, B, Cin, dtype);
@@ -771,6 +774,7 @@ extern "C" size_t disco_fused_conv_bwd_weight_workspace_bytes(const disco_psi* p
 extern "C" int disco_fused_conv_bwd_weight(const disco_psi* psi, const void* x, const void* dy, void* dW,
                                            int32_t B, int32_t Cin, int32_t Cout, disco_dtype dtype,
                                            void* workspace, size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fused_conv_bwd_weight");
   int st = check_fused_common(psi, x, dy, dW, B, Cin, Cout, dtype);
   if (st) return st;
   const size_t need = disco_fused_conv_bwd_weight_workspace_bytes(psi, B, Cin, Cout, dtype);
@@ -898,6 +902,7 @@ int noalloc_scratch(void** out) {
 extern "C" int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const void* dy, const void* W,
                                                   void* gx, int32_t B, int32_t Cin, int32_t Cout,
                                                   disco_dtype dtype, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fused_conv_bwd_input_noalloc");
   int st = check_fused_common(psi, dy, W, gx, B, Cin, Cout, dtype);
   if (st) return st;
   const size_t need = disco_fused_conv_bwd_input_workspace_bytes(psi, B, Cin, dtype);

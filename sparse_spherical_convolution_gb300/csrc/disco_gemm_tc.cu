@@ -557,7 +557,9 @@ int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, 
   g.P = P;
   g.Kt = Kt;
   g.Nt = Nt;
-  g.NB = kBMN ? (Nt >= 256 ? 256 : (Nt + 63) / 64 * 64) : (Nt + 15) / 16 * 16;
+  // outputs per tile: at most 256 (one TMEM accumulator); more outputs take
+  // more tiles along n
+  g.NB = kBMN ? (Nt >= 256 ? 256 : (Nt + 63) / 64 * 64) : (Nt >= 256 ? 256 : (Nt + 15) / 16 * 16);
   g.mt = (int)((P + kBM - 1) / kBM);
   g.nt = (Nt + g.NB - 1) / g.NB;
   g.B = B;
@@ -596,7 +598,7 @@ bool gemm_tc_supported(int64_t P, int Kt, int Nt) {
 
 int einsum_tensor_core(const void* X, const void* W, void* y, int B, int CK, int Cout, int64_t P, cudaStream_t st,
                        bool f16) {
-  if (!gemm_tc_supported(P, CK, Cout) || Cout > 256) return DISCO_ERR_UNSUPPORTED;
+  if (!gemm_tc_supported(P, CK, Cout)) return DISCO_ERR_UNSUPPORTED;
   return launch_gemm<false>(X, W, y, B, CK, Cout, P, st, nullptr, f16);
 }
 

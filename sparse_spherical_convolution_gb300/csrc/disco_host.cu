@@ -178,10 +178,12 @@ extern "C" size_t disco_host_workspace_bytes(const disco_psi* psi, int32_t B, in
 
 extern "C" int disco_fwd_host(const disco_psi* psi, const void* x_host, void* X_host, int32_t B, int32_t C,
                               disco_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_fwd_host");
   return contract_host(true, psi, x_host, X_host, B, C, dtype, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 extern "C" int disco_bwd_host(const disco_psi* psi, const void* G_host, void* gx_host, int32_t B, int32_t C,
                               disco_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_bwd_host");
   return contract_host(false, psi, G_host, gx_host, B, C, dtype, workspace, workspace_bytes, (cudaStream_t)stream);
 }

@@ -5,11 +5,22 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "disco.h"
 
 namespace disco {
+
+// An NVTX range around one C-ABI call, so that a profiler timeline that
+// records NVTX shows each call by name (header-only NVTX: no library to link;
+// without a profiler attached the push and pop return at once).
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
 
 // Records `msg` (printf-style) as this thread's last error and returns `st`.
 int fail(int st, const char* fmt, ...);

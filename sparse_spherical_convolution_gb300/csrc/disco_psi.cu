@@ -722,6 +722,7 @@ extern "C" int disco_psi_workspace_bytes(const disco_grid* grid_in, const disco_
 extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_out,
                               const disco_basis* basis, void* workspace, size_t workspace_bytes,
                               void* stream, disco_psi* psi) {
+  disco::NvtxScope nvtx_scope("disco_psi_plan");
   PsiGeom g;
   int st = make_geom(grid_in, grid_out, basis, &g);
   if (st) return st;
@@ -804,6 +805,7 @@ extern "C" int disco_psi_plan(const disco_grid* grid_in, const disco_grid* grid_
 
 extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t bytes, void* workspace,
                                        size_t workspace_bytes, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_build_psi_kpacked");
   if (!psi) return fail(DISCO_ERR_INVALID_ARG, "psi is null");
   PsiGeom g;
   int st = make_geom(&psi->grid_in, &psi->grid_out, &psi->basis, &g);
@@ -877,6 +879,7 @@ extern "C" int disco_build_psi_kpacked(disco_psi* psi, void* buffer, size_t byte
 
 extern "C" int disco_psi_export_kpacked(const disco_psi* psi, int64_t* pack_idx, float* pack_val,
                                         int64_t* pack_count, int32_t nbr_pad, void* stream) {
+  disco::NvtxScope nvtx_scope("disco_psi_export_kpacked");
   int st = check_psi(psi);
   if (st) return st;
   if ((st = check_device())) return st;

@@ -76,9 +76,10 @@ WORKLOADS = {
 ORDER = list(WORKLOADS)
 LARGEST = ORDER[-1]
 
-# The benchmark shapes the DISCO Kernel Development Guide lists (§benchmark
-# shapes), on Legendre-Gauss grids (poles = 2) with theta_cutoff = 0.017 and
-# kernel_shape (3, 3).  The page's "harmonic" basis and "mean" normalisation
+# The benchmark shapes the DISCO Kernel Development Guide lists (§Profiling /
+# Serial Benchmarks: 256 and 512 channels on 360 x 720, and 80 -> 512
+# channels from 721 x 1440 to 360 x 720), on Legendre-Gauss grids (poles = 2)
+# with theta_cutoff = 0.017 and kernel_shape (3, 3).  The page's "harmonic" basis and "mean" normalisation
 # are not defined there; this library's anisotropic basis (3 radial hats x
 # {1, cos, sin}, K = 9) and per-ring normalisation stand in.  B is not given:
 # 1.  The 721-row equiangular input includes the poles.  Parity-test cases,
@@ -88,8 +89,10 @@ PAGE_WORKLOADS = {
     for w in [
         Workload("page_self_256x360x720_gauss", 1, 256, 256, (360, 720, 2), (360, 720, 2), ANISO, 3,
                  0.017, "bf16", 5, ("fused", "fused_bwd")),
+        Workload("page_self_512x360x720_gauss", 1, 512, 512, (360, 720, 2), (360, 720, 2), ANISO, 3,
+                 0.017, "bf16", 7, ("fused", "fused_bwd")),
         Workload("page_down_80x721x1440_to_360x720_gauss", 1, 80, 512, (721, 1440, 1), (360, 720, 2),
-                 ANISO, 3, 0.017, "bf16", 6, ("fwd", "bwd")),
+                 ANISO, 3, 0.017, "bf16", 6, ("fwd", "bwd", "fused", "fused_bwd")),
     ]
 }
 

@@ -84,7 +84,7 @@ def test_fp16_fused_and_gradients(lib, case):
     dy = _gen((B, Cout, go[0], go[1]), g)
     xd, Wd, dyd = x.cuda(), W.cuda(), dy.cuda()
     y = torch.full((B, Cout, go[0], go[1]), float("nan"), dtype=H, device="cuda")
-    ws = torch.empty(lib.disco_fused_conv_workspace_bytes(psi.c, B, Cin, lib.DISCO_F16), dtype=torch.uint8,
+    ws = torch.empty(lib.disco_fused_conv_workspace_bytes(psi.c, B, Cin, Cout, lib.DISCO_F16), dtype=torch.uint8,
                      device="cuda")
     lib.disco_fused_conv(psi.c, xd, Wd, y, B, Cin, Cout, ws)
     gx = torch.full((B, Cin, gi[0], gi[1]), float("nan"), dtype=H, device="cuda")
@@ -143,7 +143,7 @@ def test_fp16_fused_shape_rules(lib):
     x = torch.zeros((1, 16, 16, 36), dtype=H, device="cuda")
     W = torch.zeros((16, 16, 3), dtype=H, device="cuda")
     y = torch.zeros((1, 16, 16, 36), dtype=H, device="cuda")
-    assert lib.disco_fused_conv_workspace_bytes(psi36.c, 1, 16, lib.DISCO_F16) == 0
+    assert lib.disco_fused_conv_workspace_bytes(psi36.c, 1, 16, 16, lib.DISCO_F16) == 0
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_fused_conv(psi36.c, x, W, y, 1, 16, 16)
     assert e.value.status == -2

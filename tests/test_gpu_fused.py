@@ -50,7 +50,7 @@ def _inputs(B, Cin, Cout, K, gi, go, seed):
 
 def _run_fused(lib, psi, x, W, B, Cin, Cout, go):
     y = torch.full((B, Cout, go[0], go[1]), float("nan"), dtype=BF, device="cuda")
-    nws = lib.disco_fused_conv_workspace_bytes(psi.c, B, Cin)
+    nws = lib.disco_fused_conv_workspace_bytes(psi.c, B, Cin, Cout)
     ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda") if nws else None
     lib.disco_fused_conv(psi.c, x, W, y, B, Cin, Cout, ws)
     return y
@@ -119,7 +119,8 @@ def test_fused_workload_full(lib):
 
 
 @pytest.mark.parametrize("name", ["fused_bwd_361x720", "down_fused_bwd_721x1440_to_361x720",
-                                  "page_self_256x360x720_gauss"])
+                                  "page_self_256x360x720_gauss", "page_self_512x360x720_gauss",
+                                  "page_down_80x721x1440_to_360x720_gauss"])
 def test_fused_workload_sampled_full_size(lib, name):
     w = WORKLOADS[name] if name in WORKLOADS else PAGE_WORKLOADS[name]
     inp = make_inputs(w)
@@ -164,7 +165,7 @@ def test_fused_rejects_unsupported(lib):
     psi36 = lib.Psi((16, 36, 0), (16, 36, 0), 0, 3, 2 * math.pi / 16)  # on-chip path
     x36 = torch.zeros((1, 8, 16, 36), dtype=BF, device="cuda")
     y36 = torch.zeros((1, 8, 16, 36), dtype=BF, device="cuda")
-    assert lib.disco_fused_conv_workspace_bytes(psi36.c, 1, 8) == 0
+    assert lib.disco_fused_conv_workspace_bytes(psi36.c, 1, 8, 8) == 0
     with pytest.raises(lib.DiscoError) as e:
         lib.disco_fused_conv(psi36.c, x36, W, y36, 1, 8, 8)  # Cin % 16 != 0 on the on-chip path
     assert e.value.status == -2
