@@ -50,7 +50,8 @@ typedef enum {
   DISCO_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
   DISCO_ERR_LAUNCH = -5,             /* a kernel launch was rejected by the runtime */
   DISCO_ERR_CUDA = -6,               /* another CUDA runtime call failed */
-  DISCO_ERR_WORKSPACE = -7           /* workspace missing or too small */
+  DISCO_ERR_WORKSPACE = -7,          /* workspace missing or too small */
+  DISCO_ERR_DEVICE_BOUNDS = -8       /* bounds-checked build: a kernel's range check failed */
 } disco_status;
 
 /* Element type of the activations (x, X, G, gx, y, dy) and of W.  The
@@ -380,12 +381,24 @@ DISCO_API int disco_bwd_host(const disco_psi* psi, const void* G_host, void* gx_
    bit 2 = one of the tensor-core forward contraction timed out,
    bit 3 = one of the tensor-core transpose contraction timed out or met an
    input-row group reading more output rows than it can hold, bit 4 = the
-   wait of disco_check_wait_timeout ran out; a kernel that times out stops
-   issuing work, frees its tensor memory and returns, leaving its outputs
-   incomplete).  clear != 0 resets the word and frees every slot of the tile
-   schedulers (see disco_check_sched_hold): call it with clear != 0 only
-   while no other thread launches work of this library on the device. */
+   wait of disco_check_wait_timeout ran out, bit 5 = in the bounds-checked
+   build, a gather index or a TMA or bulk-copy coordinate fell outside the
+   tensor it addresses; a kernel that times out stops issuing work, frees its
+   tensor memory and returns, leaving its outputs incomplete).  clear != 0
+   resets the word.  Returns DISCO_ERR_DEVICE_BOUNDS (with *flags filled in)
+   when bit 5 is set, else DISCO_OK or a CUDA error. */
 DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
+
+/* Build options of the loaded library: DISCO_BUILD_DEBUG_BOUNDS when it is the
+   bounds-checked build (compiled with -DDISCO_DEBUG_BOUNDS).  In that build
+   every kernel checks each gather index and each TMA or bulk-copy coordinate
+   against the extents of the tensor it addresses before the access; a failed
+   check skips the access (a skipped copy still completes its transaction
+   bytes, so no wait runs out), sets bit 5 of the device status word and
+   never traps.  It stands in for a memory checker on small cases; its
+   kernels are slower and it is not the product build. */
+#define DISCO_BUILD_DEBUG_BOUNDS 1
+DISCO_API int32_t disco_build_flags(void);
 
 /* Diagnostic of the failure path, asynchronous: launches one small kernel
    whose thread waits on an mbarrier phase that nothing completes, with the
@@ -396,18 +409,23 @@ DISCO_API int disco_device_status(int32_t* flags, int32_t clear);
    disco_device_status. */
 DISCO_API int disco_check_wait_timeout(uint32_t limit, void* stream);
 
-/* Diagnostic of the recovery path of the tile schedulers, synchronous.  The
-   persistent tensor-core kernels take their tiles from a counter in one of
-   1024 slots of a library-owned device table (slot = launch number mod
-   1024); a launch waits, bounded, while an earlier launch still holds its
-   slot.  This call marks the slot that the next launch will take as held by
-   a launch that never finishes, as a launch that failed part-way could leave
-   it.  The next persistent launch then gives up after its bounded wait
-   (about 3-7 s), computes nothing and sets bit 2 (forward) or bit 3
-   (transpose) of the status word; disco_device_status with clear != 0 frees
-   every slot again.  Lets a test check that a held slot is recovered; no
-   kernel faults, traps or hangs. */
-DISCO_API int disco_check_sched_hold(void);
+/* Diagnostic of the tile schedulers, synchronous.  The persistent
+   tensor-core kernels draw their tiles from one of 1024 words of a
+   library-owned device table (word = launch number mod 1024) holding the
+   tag of the launch using it, the number of its CTAs drawing, and its next
+   tile.  A CTA joins the word (its own tag: one more drawer; another tag
+   with no drawer: the word becomes its launch's, counter 0; another launch
+   still drawing: a bounded wait, after which the CTA takes no tile and sets
+   bit 2 (forward) or bit 3 (transpose) of the status word), draws with an
+   atomic add and leaves on every exit path, so no launch, failed or not,
+   leaves a word that blocks a later one.  This call first runs one thread
+   through that protocol on a private word (take-over, draws in order, a
+   sibling joining, a launch waiting while another draws, take-over once
+   the drawers left) and returns DISCO_ERR_CUDA naming the first step that
+   went wrong; it then leaves another launch's tag with its counter
+   part-way and no drawer in the words the next launch will use.  That
+   launch must compute every tile with a clear status word. */
+DISCO_API int disco_check_sched_takeover(void);
 
 #ifdef __cplusplus
 }

@@ -17,13 +17,14 @@ from . import build as _build_mod
 
 __all__ = [
     "DiscoError", "disco_grid", "disco_basis", "disco_run", "disco_psi", "Psi",
-    "disco_version", "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
+    "disco_version", "disco_build_flags", "DISCO_BUILD_DEBUG_BOUNDS", "DISCO_ERR_DEVICE_BOUNDS",
+    "disco_last_error", "disco_psi_workspace_bytes", "disco_psi_plan",
     "disco_build_psi_kpacked", "disco_psi_export_kpacked", "disco_check_wait_timeout", "disco_fwd", "disco_bwd",
     "disco_host_workspace_bytes", "disco_fwd_host", "disco_bwd_host",
     "disco_fused_conv_workspace_bytes",
     "disco_fused_conv", "disco_fused_conv_bwd_input_workspace_bytes", "disco_fused_conv_bwd_input",
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
-    "disco_fused_conv_bwd_weight", "disco_device_status", "disco_check_sched_hold", "library_path",
+    "disco_fused_conv_bwd_weight", "disco_device_status", "disco_check_sched_takeover", "library_path",
     "load_library", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = [
     "disco_fused_conv_bwd_input_noalloc", "disco_fused_conv_bwd_weight_workspace_bytes",
     "disco_fused_conv_bwd_weight", "disco_device_status", "disco_psi_export_kpacked",
     "disco_check_wait_timeout", "disco_host_workspace_bytes", "disco_fwd_host", "disco_bwd_host",
-    "disco_check_sched_hold",
+    "disco_check_sched_takeover", "disco_build_flags",
 ]
 
 
@@ -79,6 +80,10 @@ _lib = None
 
 
 def library_path() -> str:
+    """The product library, or its bounds-checked build when the environment
+    sets DISCO_GB300_BOUNDS_CHECKED=1 (a diagnostic build, see build.py)."""
+    if os.environ.get("DISCO_GB300_BOUNDS_CHECKED") == "1":
+        return _build_mod.LIB_BOUNDS
     return _build_mod.LIB
 
 
@@ -96,6 +101,8 @@ def load_library():
     PG, PB, PP = ctypes.POINTER(disco_grid), ctypes.POINTER(disco_basis), ctypes.POINTER(disco_psi)
     lib.disco_version.restype = I32
     lib.disco_version.argtypes = []
+    lib.disco_build_flags.restype = I32
+    lib.disco_build_flags.argtypes = []
     lib.disco_last_error.restype = ctypes.c_char_p
     lib.disco_last_error.argtypes = []
     lib.disco_psi_workspace_bytes.restype = ctypes.c_int
@@ -111,8 +118,8 @@ def load_library():
         getattr(lib, nm).argtypes = [PP, P, P, I32, I32, ctypes.c_int, P, SZ, P]
     lib.disco_check_wait_timeout.restype = ctypes.c_int
     lib.disco_check_wait_timeout.argtypes = [ctypes.c_uint32, P]
-    lib.disco_check_sched_hold.restype = ctypes.c_int
-    lib.disco_check_sched_hold.argtypes = []
+    lib.disco_check_sched_takeover.restype = ctypes.c_int
+    lib.disco_check_sched_takeover.argtypes = []
     lib.disco_psi_export_kpacked.restype = ctypes.c_int
     lib.disco_psi_export_kpacked.argtypes = [PP, P, P, P, I32, P]
     lib.disco_fwd.restype = ctypes.c_int
@@ -222,6 +229,15 @@ def disco_version() -> int:
     return load_library().disco_version()
 
 
+DISCO_BUILD_DEBUG_BOUNDS = 1
+DISCO_ERR_DEVICE_BOUNDS = -8
+
+
+def disco_build_flags() -> int:
+    """DISCO_BUILD_DEBUG_BOUNDS when the loaded library is the bounds-checked build."""
+    return load_library().disco_build_flags()
+
+
 def disco_last_error() -> str:
     return load_library().disco_last_error().decode()
 
@@ -287,9 +303,9 @@ def disco_check_wait_timeout(limit: int, stream=None) -> None:
     _check(load_library().disco_check_wait_timeout(limit, _stream(stream)))
 
 
-def disco_check_sched_hold() -> None:
-    """Marks the next persistent launch's scheduler slot as held (diagnostic)."""
-    _check(load_library().disco_check_sched_hold())
+def disco_check_sched_takeover() -> None:
+    """Walks the scheduler protocol, then leaves a foreign tag in the next launch's words (diagnostic)."""
+    _check(load_library().disco_check_sched_takeover())
 
 
 def disco_psi_export_kpacked(psi: disco_psi, pack_idx, pack_val, pack_count, nbr_pad: int,
@@ -375,7 +391,9 @@ def disco_fused_conv_bwd_input_noalloc(psi: disco_psi, dy, W, gx, B: int, Cin: i
 
 
 def disco_device_status(clear: bool = True) -> int:
-    """Device status word (0 = no bounded wait timed out); synchronises the device."""
+    """Device status word (0 = no bounded wait timed out); synchronises the device.
+    Raises DiscoError with status DISCO_ERR_DEVICE_BOUNDS when a range check
+    of the bounds-checked build failed."""
     v = ctypes.c_int32()
     _check(load_library().disco_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value

@@ -48,6 +48,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "disco_bounds.cuh"
 #include "disco_internal.cuh"
 #include "disco_sched.cuh"
 #include "disco_umma.cuh"
@@ -55,7 +56,7 @@
 namespace disco {
 
 __device__ int g_btc_status = 0;
-__device__ SchedSlot g_btc_sched[kSchedSlots];
+__device__ unsigned long long g_btc_sched[kSchedSlots];
 
 namespace {
 
@@ -119,6 +120,7 @@ struct BtcArgs {
   const uint16_t* gtab;
   int BC, Hin, Win, Hout, Wout, K;
   int ntx, nty, ntz;  // tiles along columns, channel blocks, row groups
+  long long ngrp_ent, ngtab;  // entries and table elements of psi (extent checks of the bounds-checked build)
   unsigned long long launch_id;  // selects the scheduler slot
   int f16;                       // G, gx and the tables are fp16 (else bf16)
 };
@@ -219,18 +221,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nsteps = min(4, (int)en.KB - 4 * c);
     const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
     mbar_expect_tx(&fullT[s], Cfg::kTabBytes);
-    bulk_copy(st + 2 * kBoxBytes + kTBytes, a.gtab + en.off + (size_t)(k * en.nch + c) * grp_block(S),
-              Cfg::kTabBytes, &fullT[s]);
+    const long long toff = (long long)en.off + (long long)(k * en.nch + c) * grp_block(S);
+    if (DISCO_IN_BOUNDS(k >= 0 && k < a.K && c >= 0 && c < en.nch && toff >= 0 && toff + grp_block(S) <= a.ngtab))
+      bulk_copy(st + 2 * kBoxBytes + kTBytes, a.gtab + toff, Cfg::kTabBytes, &fullT[s]);
+    else
+      mbar_complete_tx(&fullT[s], Cfg::kTabBytes);
     mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
     const int row = k * a.Hout + en.ho;
+    const bool rows_ok = DISCO_IN_BOUNDS(en.ho >= 0 && en.ho < a.Hout && bc0 >= 0 && bc0 < a.BC);
     for (int bb = 0; bb < nbox; ++bb) {
       const int col0 = qb - en.MW + 64 * (c + bb);
       uint8_t* dst = st + bb * kBoxBytes;
       if (!box_is_narrow(col0, a.Wout)) {
-        tma_load_3d(dst, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
+        if (DISCO_IN_BOUNDS(rows_ok && wrapc(col0, a.Wout) >= 0))
+          tma_load_3d(dst, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
+        else
+          mbar_complete_tx(&fullA[s], kBoxBytes);
       } else {
-        for (int g = 0; g < 8; ++g)
-          tma_load_3d(dst + g * kNarrowBytes, &gnarrow, wrapc(col0 + 8 * g, a.Wout), row, bc0, &fullA[s]);
+        for (int g = 0; g < 8; ++g) {
+          const int cn = wrapc(col0 + 8 * g, a.Wout);
+          if (DISCO_IN_BOUNDS(rows_ok && cn >= 0 && cn + 8 <= a.Wout))
+            tma_load_3d(dst + g * kNarrowBytes, &gnarrow, cn, row, bc0, &fullA[s]);
+          else
+            mbar_complete_tx(&fullA[s], kNarrowBytes);
+        }
       }
     }
     return true;
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int i = 0, tl = 0, done = 0;  // done: one past the last item this thread issued
       bool ok = true;
-      SchedSlot* slot = sched_claim(g_btc_sched, a.launch_id, kWaitLimit);
+      unsigned long long* slot = sched_join(g_btc_sched, a.launch_id, kWaitLimit);
       if (!slot) btc_flag(kStatusBtcTimeout);  // this CTA takes no tile
       for (; ok; ++tl) {
         const int b = tl & 1;
@@ -269,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int qb, bc0, zg;
         tile_coords<S>(a, tile, &qb, &bc0, &zg);
         const int e0 = a.grp_ptr[zg];
-        const int ne = min(a.grp_ptr[zg + 1] - e0, kMaxEnt);
+        int ne = min(a.grp_ptr[zg + 1] - e0, kMaxEnt);
+        if (!DISCO_IN_BOUNDS(zg >= 0 && zg < a.ntz && e0 >= 0 && ne >= 0 && e0 + (long long)ne <= a.ngrp_ent))
+          ne = 0;
         info_cnt[b] = ne;
         disco_grp_ent* info = infos + b * kMaxEnt;
         if (ne > 0) {
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
         drain_own(done, 0);
       }
-      if (slot) sched_release(slot);
+      if (slot) sched_leave(slot);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
@@ -504,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("bar.sync 2, 128;" ::: "memory");
           if (tid == 256) {
             const int col = S * (qb + blk * TQ);
-            if (col < a.Win && hi0 + r < a.Hin)  // else the whole piece lies outside gx
+            if (col < a.Win && hi0 + r < a.Hin &&  // else the whole piece lies outside gx
+                DISCO_IN_BOUNDS(col >= 0 && hi0 + r >= 0 && bc0 >= 0 && bc0 < a.BC))
               asm volatile(
                   "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                       reinterpret_cast<uint64_t>(&gxmap)),
@@ -595,6 +612,8 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
   a.ntx = (a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ);
   a.nty = (BC + 127) / 128;
   a.ntz = psi->ngrp;
+  a.ngrp_ent = psi->ngrp_ent;
+  a.ngtab = psi->ngtab;
   a.launch_id = next_launch_id();
   CUtensorMap wide, narrow, gxm;
   int stt = encode_g(&wide, G, a, BC, 64, true, roc);
@@ -617,26 +636,20 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
     return check_launch("disco_bwd (tensor cores) attribute");
   const long long ntiles = (long long)a.ntx * a.nty * a.ntz;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
+  if (ntiles + grid > (long long)kSchedCountMask || grid > kSchedMaxCtas)
+    return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
   kern<<<grid, kThreads, Cfg::kSmem, st>>>(wide, narrow, gxm, a);
   return check_launch("disco_bwd (tensor cores)");
 }
 
 }  // namespace
 
-// Marks the slot of launch `id` as held by a launch that never finishes, as a
-// slot left behind by a failed launch would be (diagnostic of the recovery
-// path; the next launch's claims then run out and flag the status word).
-cudaError_t btc_sched_hold(unsigned long long id) {
-  SchedSlot s{~0ull, 0, 0};
-  return cudaMemcpyToSymbol(g_btc_sched, &s, sizeof(SchedSlot), (id % kSchedSlots) * sizeof(SchedSlot));
-}
-
-// Frees every slot.  Only while no kernel of this library runs on the device
-// (disco_device_status calls it after synchronising the device): a slot that
-// a failed launch left held is then usable again.
-cudaError_t btc_sched_reset() {
-  static const SchedSlot zero[kSchedSlots] = {};
-  return cudaMemcpyToSymbol(g_btc_sched, zero, sizeof(zero));
+// Leaves in the scheduler word of launch `id` the tag of another launch with
+// its counter part-way, as any earlier launch leaves it (diagnostic: launch
+// `id` must take the word over and still compute every tile).
+cudaError_t btc_sched_plant(unsigned long long id) {
+  const unsigned long long w = sched_tag(id + kSchedSlots) | 5ull;  // no active CTA
+  return cudaMemcpyToSymbol(g_btc_sched, &w, sizeof(w), (id % kSchedSlots) * sizeof(w));
 }
 
 cudaError_t btc_status(int32_t* v, bool clear) {
@@ -665,5 +678,8 @@ int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaS
   return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st, rows_of_channels, f16)
                      : launch_btc<2>(psi, G, gx, BC, st, rows_of_channels, f16);
 }
+
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(btc_bounds)
 
 }  // namespace disco

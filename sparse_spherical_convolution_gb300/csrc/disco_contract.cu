@@ -44,6 +44,8 @@ struct ContractArgs {
   const float* hval_full;  // union layout values [nnz][Kp] (signed offsets)
   const int32_t* row_order;
   int vec_ok;  // output rows are 16-byte aligned
+  int nruns;                // runs, hval rows and union entries of psi
+  long long nhval, nnz;     // (extent checks of the bounds-checked build)
 };
 
 template <typename T>
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const ContractArgs a) 
   extern __shared__ float sm[];
   using G = FwdGather<T, K, S, ANISO>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ho = a.row_order[blockIdx.z];
+  int ho = a.row_order[blockIdx.z];
+  if (!DISCO_IN_BOUNDS(ho >= 0 && ho < a.Hout)) ho = 0;
   const int bc0 = blockIdx.y * 32;
   const int wo_blk = blockIdx.x * kTile;
   const int o0 = warp * kTW;
@@ -125,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_kernel(const ContractArgs a) 
   ga.runs = a.runs;
   ga.hval = a.hval;
   ga.Kp = a.Kp;
+  ga.nruns = a.nruns;
+  ga.nhval = a.nhval;
   float acc[K][kTW];
   G::run(acc, sm, ga, ho, wo_blk, lane, o0, threadIdx.x, 0);
 
@@ -210,11 +215,18 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) 
 #pragma unroll
     for (int t = 0; t < kBT; ++t) acc[p][t] = 0.f;
 
-  const int t_begin = a.trun_ptr[hi], t_end = a.trun_ptr[hi + 1];
+  const int t_begin = a.trun_ptr[hi];
+  int t_end = a.trun_ptr[hi + 1];
+  if (!DISCO_IN_BOUNDS(t_begin >= 0 && t_begin <= t_end && t_end <= a.nruns)) t_end = t_begin;
   for (int tr = t_begin; tr < t_end; ++tr) {
-    const disco_run run = a.runs[a.truns[tr]];
+    const int ri = a.truns[tr];
+    if (!DISCO_IN_BOUNDS(ri >= 0 && ri < a.nruns)) continue;  // the whole block skips it alike
+    const disco_run run = a.runs[ri];
     const int dlo = (run.len == a.Win) ? -(a.Win / 2) : -run.npair;
     const int dhi = dlo + run.len - 1;
+    if (!DISCO_IN_BOUNDS(run.ho >= 0 && run.ho < a.Hout && run.len >= 1 && run.e0 >= 0 &&
+                         run.e0 + (long long)run.len <= a.nnz))
+      continue;
     const int dstart = (dlo >= 0) ? (dlo & ~7) : -(((-dlo) + 7) & ~7);  // multiple of 8, <= dlo
     for (int da = dstart; da <= dhi; da += kBDC) {
       // decimated G index of (j, delta) is (j - delta)/S; over the block and chunk
@@ -231,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_kernel(const ContractArgs a) 
         for (int i = lane; i < BwdWin<T, S>::kLen; i += 32) {
           int col = g0 + i;
           if (col >= Wo) col %= Wo;
-          dst[i] = St::put((bc < a.BC) ? to_f32(src[col]) : 0.f);
+          dst[i] = St::put((bc < a.BC && DISCO_IN_BOUNDS(col >= 0 && col < Wo)) ? to_f32(src[col]) : 0.f);
         }
       }
       // psi values of the chunk, signed offsets, zero outside the run
@@ -371,6 +383,9 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   a.truns = psi->truns;
   a.hval = psi->hval;
   a.hval_full = psi->val;
+  a.nruns = (int)psi->nruns;
+  a.nhval = psi->nhval;
+  a.nnz = psi->nnz;
   a.row_order = psi->row_order;
   int elems16 = dtype == DISCO_F32 ? 4 : 8;
   a.vec_ok = ((fwd ? a.Wout : a.Win) % elems16) == 0;
@@ -390,6 +405,9 @@ int contract(bool fwd, const disco_psi* psi, const void* in, void* out, int32_t 
   return psi->s == 1 ? dispatch<__nv_bfloat16, 1>(fwd, kind, K, a, s)
                      : dispatch<__nv_bfloat16, 2>(fwd, kind, K, a, s);
 }
+
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(contract_bounds)
 
 }  // namespace disco
 

@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "disco_gather.cuh"
+#include "disco_sched.cuh"
 #include "disco_umma.cuh"
 
 namespace disco {
@@ -63,6 +64,8 @@ struct FusedArgs {
   const disco_run* runs;
   const float* hval;
   const int32_t* row_order;
+  int nruns;        // runs and hval rows of psi (extent checks of the
+  long long nhval;  // bounds-checked build)
 };
 
 template <int K, int S, bool ANISO>
@@ -99,7 +102,8 @@ __global__ void __launch_bounds__(kFThreads, 2) fused_fwd_kernel(const FusedArgs
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.z;
-  const int ho = a.row_order[blockIdx.y];
+  int ho = a.row_order[blockIdx.y];
+  if (!DISCO_IN_BOUNDS(ho >= 0 && ho < a.Hout)) ho = 0;
   const int wo_blk = blockIdx.x * kFNW;
   const int NC = a.Cin / kFCC;
   const uint32_t ncols = tmem_cols_for(a.MT * kFNW);
@@ -191,6 +195,8 @@ __global__ void __launch_bounds__(kFThreads, 2) fused_fwd_kernel(const FusedArgs
     ga.runs = a.runs;
     ga.hval = a.hval;
     ga.Kp = a.Kp;
+    ga.nruns = a.nruns;
+    ga.nhval = a.nhval;
     bool ok = true;
     for (int ci = 0; ci < NC && ok; ++ci) {
       ga.bc0 = b * a.Cin + ci * kFCC;
@@ -689,6 +695,8 @@ extern "C" int disco_fused_conv(const disco_psi* psi, const void* x, const void*
   a.runs = psi->runs;
   a.hval = psi->hval;
   a.row_order = psi->row_order;
+  a.nruns = (int)psi->nruns;
+  a.nhval = psi->nhval;
   return psi->s == 1 ? dispatch_fused<1>(psi->basis.kind, psi->K, a, s)
                      : dispatch_fused<2>(psi->basis.kind, psi->K, a, s);
 }
@@ -828,21 +836,78 @@ extern "C" int disco_device_status(int32_t* flags, int32_t clear) {
   if (e == cudaSuccess) e = tc_status(flags, clear != 0);
   if (e == cudaSuccess) e = btc_status(flags, clear != 0);
   if (e == cudaSuccess) e = gemm_status(flags, clear != 0);
-  // a launch that failed may have left its scheduler slot held; with the
-  // device synchronised no kernel of this library runs, so every slot is free
-  if (e == cudaSuccess && clear) e = fwd_sched_reset();
-  if (e == cudaSuccess && clear) e = btc_sched_reset();
+  int32_t bounds = 0;
+  for (auto fn : {contract_bounds, psi_bounds, tc_bounds, btc_bounds, gemm_bounds, fused_bounds})
+    if (e == cudaSuccess) e = fn(&bounds, clear != 0);
+  *flags |= bounds;
   if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
+  if (bounds & kStatusBounds)
+    return fail(DISCO_ERR_DEVICE_BOUNDS, "a range check of the bounds-checked build failed (access skipped)");
   return DISCO_OK;
 }
 
-extern "C" int disco_check_sched_hold(void) {
+extern "C" int32_t disco_build_flags(void) {
+#ifdef DISCO_DEBUG_BOUNDS
+  return DISCO_BUILD_DEBUG_BOUNDS;
+#else
+  return 0;
+#endif
+}
+
+namespace disco {
+namespace {
+
+// One thread walks the scheduler protocol (disco_sched.cuh) on a private word,
+// playing the CTAs of two launches; ids are multiples of kSchedSlots so the
+// word is entry 0 of the one-entry table.
+__device__ unsigned long long g_sched_walk[1];
+__device__ int g_sched_walk_out[9];
+
+__global__ void sched_walk_kernel() {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  constexpr unsigned long long L1 = 1 * kSchedSlots, L2 = 2 * kSchedSlots;
+  unsigned long long* const t = g_sched_walk;
+  t[0] = sched_tag(4 * kSchedSlots) | 7ull;  // left by an earlier launch, no active CTA
+  int* o = g_sched_walk_out;
+  unsigned long long* a = sched_join(t, L1, 4);       // launch 1 takes the word
+  o[0] = a != nullptr;                                // 1
+  o[1] = a ? sched_next(a) : -1;                      // 0
+  o[2] = a ? sched_next(a) : -1;                      // 1
+  unsigned long long* b = sched_join(t, L1, 4);       // a sibling joins
+  o[3] = b ? sched_next(b) : -1;                      // 2
+  o[4] = sched_join(t, L2, 4) == nullptr;             // launch 2 waits while launch 1 draws: 1
+  if (a) sched_leave(a);
+  if (b) sched_leave(b);
+  unsigned long long* c = sched_join(t, L2, 4);       // launch 1 gone: launch 2 takes the word
+  o[5] = c ? sched_next(c) : -1;                      // 0
+  o[6] = sched_join(t, L1, 4) == nullptr;             // a late CTA of launch 1 waits: 1
+  if (c) sched_leave(c);
+  unsigned long long* d = sched_join(t, L1, 4);       // ... and takes the word back once free
+  o[7] = d ? sched_next(d) : -1;                      // 0
+  if (d) sched_leave(d);
+  o[8] = t[0] == (sched_tag(L1) | 1ull);              // no active CTA left: 1
+}
+
+}  // namespace
+}  // namespace disco
+
+extern "C" int disco_check_sched_takeover(void) {
   int st = check_device();
   if (st) return st;
+  sched_walk_kernel<<<1, 32>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  int got[9];
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(got, g_sched_walk_out, sizeof(got));
+  if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "scheduler walk: %s", cudaGetErrorString(e));
+  const int want[9] = {1, 0, 1, 2, 1, 0, 1, 0, 1};
+  for (int k = 0; k < 9; ++k)
+    if (got[k] != want[k])
+      return fail(DISCO_ERR_CUDA, "scheduler walk: step %d drew %d, expected %d", k, got[k], want[k]);
   const unsigned long long id = peek_launch_id();
-  cudaError_t e = fwd_sched_hold(id);
-  if (e == cudaSuccess) e = btc_sched_hold(id);
-  if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "scheduler slot: %s", cudaGetErrorString(e));
+  e = fwd_sched_plant(id);
+  if (e == cudaSuccess) e = btc_sched_plant(id);
+  if (e != cudaSuccess) return fail(DISCO_ERR_CUDA, "scheduler word: %s", cudaGetErrorString(e));
   return DISCO_OK;
 }
 
@@ -897,6 +962,9 @@ int noalloc_scratch(void** out) {
 }
 
 }  // namespace
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(fused_bounds)
+
 }  // namespace disco
 
 extern "C" int disco_fused_conv_bwd_input_noalloc(const disco_psi* psi, const void* dy, const void* W,

@@ -37,6 +37,7 @@
 
 #include <cstring>
 
+#include "disco_bounds.cuh"
 #include "disco_internal.cuh"
 #include "disco_sched.cuh"
 #include "disco_umma.cuh"
@@ -100,6 +101,9 @@ struct TcArgs {
   const int32_t* ftab_off;
   const uint16_t* ftab;  // per run: K rows of TL = roundup8(len + 16), psi_k(delta) at 8 + delta - dlo
   int BC, Hout, Wout, Win;
+  int Hin;            // input rows (extent checks of the bounds-checked build)
+  int nruns;          // runs, and ftab elements, of psi (the same checks)
+  long long nftab;
   int TLB;            // table row capacity (>= every run's row length)
   int tma_store;      // X written by TMA stores (W_out % 8 == 0 and W_out >= one tile's columns)
   int f16;            // x, X and the tables are fp16 (else bf16)
@@ -178,10 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t tab_bytes = Cfg::tab_bytes(a.TLB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ho = a.row_order[blockIdx.z];
+  int ho = a.row_order[blockIdx.z];
+  if (!DISCO_IN_BOUNDS(ho >= 0 && ho < a.Hout)) ho = 0;
   const int bc0 = blockIdx.y * 128;
   const int wc = blockIdx.x * (kTW * NT);
-  const int r_begin = a.run_ptr[ho], r_end = a.run_ptr[ho + 1];
+  const int r_begin = a.run_ptr[ho];
+  int r_end = a.run_ptr[ho + 1];
+  if (!DISCO_IN_BOUNDS(r_begin >= 0 && r_begin <= r_end && r_end <= a.nruns)) r_end = r_begin;
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -229,7 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t bytes = (uint32_t)K * g.TL * 2;
           mbar_expect_tx(&tfull[b], bytes);
-          bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+          if (DISCO_IN_BOUNDS(g.TL <= a.TLB && a.ftab_off[r] >= 0 && a.ftab_off[r] + (long long)K * g.TL <= a.nftab))
+            bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+          else
+            mbar_complete_tx(&tfull[b], bytes);
         }
         for (int c = 0; c * kCK < g.KS; ++c, ++i) {
           const int s = i % STAGES;
@@ -246,12 +256,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
           for (int bb = 0; bb < nbox; ++bb) {
             const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
+            const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
             if (col + 64 <= a.Win) {
-              tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+              if (DISCO_IN_BOUNDS(rows_ok && col >= 0))
+                tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+              else
+                mbar_complete_tx(&fullA[s], kBoxBytes);
             } else {  // crosses the longitude seam: 8 wrapped narrow boxes
-              for (int gi = 0; gi < 8; ++gi)
-                tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow,
-                            wrap_col(col + 8 * gi, a.Win), g.hi, bc0, &fullA[s]);
+              for (int gi = 0; gi < 8; ++gi) {
+                const int cn = wrap_col(col + 8 * gi, a.Win);
+                if (DISCO_IN_BOUNDS(rows_ok && cn >= 0 && cn + 8 <= a.Win))
+                  tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow, cn, g.hi, bc0, &fullA[s]);
+                else
+                  mbar_complete_tx(&fullA[s], kNarrowBytes);
+              }
             }
           }
         }
@@ -403,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.sync 2, 128;" ::: "memory");
         if (warp == 4 && lane == 0) {
           for (int k = 0; k < K; ++k)
-            asm volatile(
+            if (DISCO_IN_BOUNDS(wc >= 0 && wc < a.Wout && ho >= 0 && ho < a.Hout && bc0 >= 0 && bc0 < a.BC))
+              asm volatile(
                 "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                     reinterpret_cast<uint64_t>(&outmap)),
                 "r"(wc), "r"(k * a.Hout + ho), "r"(bc0), "r"(smem_u32(smem + (size_t)k * 128 * Cfg::kOutRow))
@@ -472,7 +491,7 @@ constexpr int kPThreads = 384;
 constexpr int kPEpiThreads = 128;  // warps 8-11
 constexpr int kRing = 4;           // tile indices in flight between the producer and the consumers
 
-__device__ SchedSlot g_fwd_sched[kSchedSlots];
+__device__ unsigned long long g_fwd_sched[kSchedSlots];
 
 // Consumer side of the tile ring: the tl-th tile index (-1 once there are no
 // more), or -2 when the wait timed out or the CTA aborts.  Every consumer
@@ -531,6 +550,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int r = t / ntx;
     *bc0 = (r % nty) * 128;
     *ho = a.row_order[r / nty];
+    if (!DISCO_IN_BOUNDS(*ho >= 0 && *ho < a.Hout)) *ho = 0;
+  };
+  // runs of output row ho; every role clips a bad range the same way
+  auto row_runs = [&](int ho, int* rb, int* re) {
+    *rb = a.run_ptr[ho];
+    *re = a.run_ptr[ho + 1];
+    if (!DISCO_IN_BOUNDS(*rb >= 0 && *rb <= *re && *re <= a.nruns)) *re = *rb;
   };
 
   if (tid == 0) {
@@ -566,7 +592,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       int i = 0, rl = 0;
       bool ok = true;
-      SchedSlot* slot = sched_claim(g_fwd_sched, a.launch_id, kWaitLimit);
+      unsigned long long* slot = sched_join(g_fwd_sched, a.launch_id, kWaitLimit);
       if (!slot) tc_flag(kStatusTcTimeout);  // this CTA takes no tile
       for (int tl = 0; ok; ++tl) {
         const int rb = tl % kRing;
@@ -580,8 +606,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (t >= ntiles) break;
         int ho, bc0, wc;
         coords(t, &ho, &bc0, &wc);
-        const int r_end = a.run_ptr[ho + 1];
-        for (int r = a.run_ptr[ho]; r < r_end && ok; ++r, ++rl) {
+        int r_beg, r_end;
+        row_runs(ho, &r_beg, &r_end);
+        for (int r = r_beg; r < r_end && ok; ++r, ++rl) {
           const RunGeom g = run_geom<S>(a.runs[r], a.Win);
           const int u0 = S * wc - g.M;
           const int b = rl & 1;
@@ -591,7 +618,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           const uint32_t bytes = (uint32_t)K * g.TL * 2;
           mbar_expect_tx(&tfull[b], bytes);
-          bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+          if (DISCO_IN_BOUNDS(g.TL <= a.TLB && a.ftab_off[r] >= 0 && a.ftab_off[r] + (long long)K * g.TL <= a.nftab))
+            bulk_copy(tabs + b * tab_bytes, a.ftab + a.ftab_off[r], bytes, &tfull[b]);
+          else
+            mbar_complete_tx(&tfull[b], bytes);
           for (int c = 0; c * kCK < g.KS; ++c, ++i) {
             const int s = i % STAGES;
             if ((i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, kWaitLimit)) || *abort_flag) {
@@ -604,12 +634,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
             for (int bb = 0; bb < nbox; ++bb) {
               const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
+              const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
               if (col + 64 <= a.Win) {
-                tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+                if (DISCO_IN_BOUNDS(rows_ok && col >= 0))
+                  tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
+                else
+                  mbar_complete_tx(&fullA[s], kBoxBytes);
               } else {
-                for (int gi = 0; gi < 8; ++gi)
-                  tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow, wrap_col(col + 8 * gi, a.Win),
-                              g.hi, bc0, &fullA[s]);
+                for (int gi = 0; gi < 8; ++gi) {
+                  const int cn = wrap_col(col + 8 * gi, a.Win);
+                  if (DISCO_IN_BOUNDS(rows_ok && cn >= 0 && cn + 8 <= a.Win))
+                    tma_load_3d(sA + bb * kBoxBytes + gi * kNarrowBytes, &xnarrow, cn, g.hi, bc0, &fullA[s]);
+                  else
+                    mbar_complete_tx(&fullA[s], kNarrowBytes);
+                }
               }
             }
           }
@@ -627,7 +665,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mbar_wait(&tfull[lr & 1], (lr >> 1) & 1, kWaitLimit);
         }
       }
-      if (slot) sched_release(slot);
+      if (slot) sched_leave(slot);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
@@ -650,8 +688,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
         tc_fence_after();
         bool first = true;
-        const int r_end = a.run_ptr[ho + 1];
-        for (int r = a.run_ptr[ho]; r < r_end && ok; ++r) {
+        int r_beg, r_end;
+        row_runs(ho, &r_beg, &r_end);
+        for (int r = r_beg; r < r_end && ok; ++r) {
           const RunGeom g = run_geom<S>(a.runs[r], a.Win);
           for (int c = 0; c * kCK < g.KS; ++c, ++i) {
             const int s = i % STAGES;
@@ -712,8 +751,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!ok || t == -1) break;
       int ho, bc0, wc;
       coords(t, &ho, &bc0, &wc);
-      const int r_end = a.run_ptr[ho + 1];
-      for (int r = a.run_ptr[ho]; r < r_end && ok; ++r, ++rl) {
+      int r_beg, r_end;
+      row_runs(ho, &r_beg, &r_end);
+      for (int r = r_beg; r < r_end && ok; ++r, ++rl) {
         const RunGeom g = run_geom<S>(a.runs[r], a.Win);
         const int tb = rl & 1;
         const uint16_t* tab = reinterpret_cast<const uint16_t*>(tabs + tb * tab_bytes);
@@ -775,7 +815,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (t == -1) break;
       int ho, bc0, wc;
       coords(t, &ho, &bc0, &wc);
-      const bool any = a.run_ptr[ho + 1] > a.run_ptr[ho];
+      int r_beg, r_end;
+      row_runs(ho, &r_beg, &r_end);
+      const bool any = r_end > r_beg;
       bool fin = mbar_wait(acc_full, tl & 1, kWaitLimit) && !*abort_flag;
       fin = group_all_b(fin, 2, kPEpiThreads);  // one decision for the 4 warps (named barriers below)
       if (!fin) {
@@ -812,7 +854,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         fence_proxy_async_smem();
         asm volatile("bar.sync 2, 128;" ::: "memory");
         if (tid == 256) {
-          asm volatile(
+          if (DISCO_IN_BOUNDS(wc >= 0 && wc < a.Wout && ho >= 0 && ho < a.Hout && bc0 >= 0 && bc0 < a.BC))
+            asm volatile(
               "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                   reinterpret_cast<uint64_t>(&outmap)),
               "r"(wc), "r"(k * a.Hout + ho), "r"(bc0), "r"(smem_u32(pb))
@@ -889,6 +932,9 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
   a.Wout = psi->grid_out.nlon;
   a.Win = Win;
   a.TLB = (Win + 16 + 7) & ~7;  // a run is at most one ring long
+  a.Hin = Hin;
+  a.nruns = (int)psi->nruns;
+  a.nftab = psi->nftab;
   if (!a.ftab || !psi->ftab_off) return DISCO_ERR_UNSUPPORTED;
   const bool fit3 = TcCfg<K, S, 3>::smem(a.TLB) <= kMaxSmem;
   const bool fit2 = TcCfg<K, S, 2>::smem(a.TLB) <= kMaxSmem;
@@ -927,8 +973,9 @@ int launch_tc(const disco_psi* psi, const void* x, void* X, int BC, cudaStream_t
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return check_launch("disco_fwd (tensor cores) attribute");
     const long long ntiles = (long long)((a.Wout + kTW * NT3 - 1) / (kTW * NT3)) * ((BC + 127) / 128) * a.Hout;
-    if (ntiles > 0x7fffffffLL) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
     const int grid = (int)(ntiles < sm_count_f() ? ntiles : sm_count_f());
+    if (ntiles + grid > (long long)kSchedCountMask || grid > kSchedMaxCtas)
+      return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
     a.launch_id = next_launch_id();
     kern<<<grid, kPThreads, smem, st>>>(map, nmap, omap, a);
     return check_launch("disco_fwd (tensor cores)");
@@ -945,20 +992,12 @@ bool fits_tc(const disco_psi* psi) {
 
 }  // namespace
 
-// Marks the slot of launch `id` as held by a launch that never finishes, as a
-// slot left behind by a failed launch would be (diagnostic of the recovery
-// path; the next launch's claims then run out and flag the status word).
-cudaError_t fwd_sched_hold(unsigned long long id) {
-  SchedSlot s{~0ull, 0, 0};
-  return cudaMemcpyToSymbol(g_fwd_sched, &s, sizeof(SchedSlot), (id % kSchedSlots) * sizeof(SchedSlot));
-}
-
-// Frees every slot.  Only while no kernel of this library runs on the device
-// (disco_device_status calls it after synchronising the device): a slot that
-// a failed launch left held is then usable again.
-cudaError_t fwd_sched_reset() {
-  static const SchedSlot zero[kSchedSlots] = {};
-  return cudaMemcpyToSymbol(g_fwd_sched, zero, sizeof(zero));
+// Leaves in the scheduler word of launch `id` the tag of another launch with
+// its counter part-way, as any earlier launch leaves it (diagnostic: launch
+// `id` must take the word over and still compute every tile).
+cudaError_t fwd_sched_plant(unsigned long long id) {
+  const unsigned long long w = sched_tag(id + kSchedSlots) | 5ull;  // no active CTA
+  return cudaMemcpyToSymbol(g_fwd_sched, &w, sizeof(w), (id % kSchedSlots) * sizeof(w));
 }
 
 // Reads (and optionally clears) this unit's status word; the caller has
@@ -1015,5 +1054,8 @@ int fwd_tensor_core(const disco_psi* psi, const void* x, void* X, int BC, cudaSt
 #undef DISCO_TCASE
   return DISCO_ERR_UNSUPPORTED;
 }
+
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(tc_bounds)
 
 }  // namespace disco

@@ -19,6 +19,7 @@
 // window per side.
 #pragma once
 
+#include "disco_bounds.cuh"
 #include "disco_internal.cuh"
 
 namespace disco {
@@ -61,6 +62,8 @@ struct RowGather {
     const disco_run* runs;
     const float* hval;
     int Kp;
+    int nruns;        // runs and hval rows of psi (extent checks of the
+    long long nhval;  // bounds-checked build)
   };
 
   __device__ static void run(float (&acc)[K][TW], float* sm, const Args& a, int ho, int wo_blk,
@@ -73,9 +76,15 @@ struct RowGather {
       for (int t = 0; t < TW; ++t) acc[k][t] = 0.f;
     const int P0 = S * wo_blk;
     const int W = a.W;
-    const int r_begin = a.run_ptr[ho], r_end = a.run_ptr[ho + 1];
+    const int r_begin = a.run_ptr[ho];
+    int r_end = a.run_ptr[ho + 1];
+    if (!DISCO_IN_BOUNDS(r_begin >= 0 && r_begin <= r_end && r_end <= a.nruns)) r_end = r_begin;
     for (int r = r_begin; r < r_end; ++r) {
       const disco_run run = a.runs[r];
+      // (every thread of the group reads the same run and skips it alike)
+      if (!DISCO_IN_BOUNDS(run.hi >= 0 && run.hi < a.Hin && run.D >= 0 && run.hoff >= 0 &&
+                           run.hoff + (long long)run.D + 1 <= a.nhval))
+        continue;
       const int steps = run.D + 1;
       const int dc = min(kDCMax, (steps + 7) & ~7);
       const T* xrow = a.x + (size_t)run.hi * W;
@@ -103,7 +112,7 @@ struct RowGather {
             for (int j = tid & 31; j < len_p; j += 32) {
               int col = base + j;
               if (col >= W) col %= W;
-              dst[j] = (bc < a.BC) ? to_f32(src[col]) : 0.f;
+              dst[j] = (bc < a.BC && DISCO_IN_BOUNDS(col >= 0 && col < W)) ? to_f32(src[col]) : 0.f;
             }
           }
           for (int i = tid; i < dc * K; i += NT) {

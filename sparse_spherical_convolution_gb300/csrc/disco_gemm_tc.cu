@@ -26,6 +26,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "disco_bounds.cuh"
 #include "disco_internal.cuh"
 #include "disco_umma.cuh"
 
@@ -169,6 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + s * kStageBytes;
           uint8_t* sb = sa + kABytes;
           mbar_expect_tx(&full[s], kABytes + bbytes);
+          // the tile's origin lies inside the operands (boxes past the ends of a
+          // ragged tail are read as zeros by the copy engine, by design)
+          if (!DISCO_IN_BOUNDS(p0 >= 0 && p0 < a.P && kc * kBK < a.Kt && b >= 0 && b < a.B && n0 >= 0 &&
+                               n0 < a.Nt)) {
+            mbar_complete_tx(&full[s], kABytes + bbytes);
+            continue;
+          }
           tma_load_3d(sa, &amap, p0, kc * kBK, b, &full[s]);
           tma_load_3d(sa + kABytes / 2, &amap, p0 + 64, kc * kBK, b, &full[s]);
           if (kBMN) {
@@ -283,11 +291,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t pp = pw + seg * 8;  // P % 8 == 0: a segment is all in or all out
           if (n < a.Nt && pp < a.P) {
             __nv_bfloat16* dst;
-            if (a.ctK > 0)  // W % 8 == 0: the 8 pixels lie in one row
+            bool inside;
+            if (a.ctK > 0) {  // W % 8 == 0: the 8 pixels lie in one row
               dst = a.out + (((int64_t)rk[h] * a.ctH + rho) * BC + (int64_t)b * a.ctC + rc[h]) * a.ctW + rwo;
-            else
+              inside = DISCO_IN_BOUNDS(rk[h] >= 0 && rk[h] < a.ctK && rho >= 0 && rho < a.ctH && rc[h] >= 0 &&
+                                       rc[h] < a.ctC && b < a.B && rwo >= 0 && rwo + 8 <= a.ctW);
+            } else {
               dst = ob + (size_t)n * a.P + pp;
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(stg + row * 32 + seg * 8);
+              inside = DISCO_IN_BOUNDS(b >= 0 && b < a.B && pp >= 0 && pp + 8 <= a.P);
+            }
+            if (inside) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(stg + row * 32 + seg * 8);
           }
         }
         __syncwarp();
@@ -399,8 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // rows of a box past the tensor (o >= Cout, n >= Nt) keep stale values:
           // they only reach accumulator rows / columns that are never reduced
           mbar_expect_tx(&full[s], a.abytes + a.bbytes);
-          tma_load_3d(sa, &amap, p0, o0, b, &full[s]);
-          tma_load_3d(sa + kABytes, &bmap, p0, n0, b, &full[s]);
+          if (DISCO_IN_BOUNDS(p0 >= 0 && p0 < a.P && o0 >= 0 && o0 < a.Cout && n0 >= 0 && n0 < a.Nt && b >= 0 &&
+                              b < a.B)) {
+            tma_load_3d(sa, &amap, p0, o0, b, &full[s]);
+            tma_load_3d(sa + kABytes, &bmap, p0, n0, b, &full[s]);
+          } else {
+            mbar_complete_tx(&full[s], a.abytes + a.bbytes);
+          }
         }
       }
       if (!ok) {
@@ -469,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool empty_split = q1 <= q0;  // no reduction steps: the partial is zero
       const int row = o0 + q4 * 32 + lane;
       float* dst = a.part + ((size_t)sp * a.mt * kBM + row) * ((size_t)a.nt * a.NB) + n0;
-      for (int c0 = 0; c0 < a.NB; c0 += 16) {
+      const bool inside = DISCO_IN_BOUNDS(sp >= 0 && sp < a.nsplit && row >= 0 && row < a.mt * kBM && n0 >= 0 &&
+                                          n0 + a.NB <= a.nt * a.NB);
+      for (int c0 = 0; c0 < a.NB && inside; c0 += 16) {
         float v[16];
         if (!empty_split) {
           tmem_ld16(tmem + ab * 256 + ((uint32_t)(q4 * 32) << 16) + c0, v);
@@ -500,6 +520,7 @@ __global__ void dw_reduce_kernel(const float* part, uint16_t* dW, int Cout, int 
   if (i >= (int64_t)Cout * Nt) return;
   const int o = (int)(i / Nt), n = (int)(i - (int64_t)o * Nt);
   float acc = 0.f;
+  if (!DISCO_IN_BOUNDS(o < rows && n < cols)) return;
   for (int sp = 0; sp < nsplit; ++sp) acc += part[((size_t)sp * rows + o) * cols + n];
   dW[i] = round_16(acc, f16);
 }
@@ -700,5 +721,8 @@ cudaError_t gemm_status(int32_t* v, bool clear) {
   *v |= t;
   return e;
 }
+
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(gemm_bounds)
 
 }  // namespace disco

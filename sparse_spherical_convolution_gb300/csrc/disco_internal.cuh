@@ -47,13 +47,10 @@ int check_dev_ptr(const void* p, const char* name);
 // device index, so a context that was reset and re-created is seen as new.
 void* current_context();
 
-// Scheduler tables of the persistent kernels (disco_sched.cuh): mark the slot
-// of launch `id` as held by a launch that never finishes (a diagnostic), or
-// free every slot (only while no kernel of this library runs on the device).
-cudaError_t fwd_sched_hold(unsigned long long id);
-cudaError_t fwd_sched_reset();
-cudaError_t btc_sched_hold(unsigned long long id);
-cudaError_t btc_sched_reset();
+// Scheduler words of the persistent kernels (disco_sched.cuh): leave another
+// launch's tag, counter part-way, in the word that launch `id` will use.
+cudaError_t fwd_sched_plant(unsigned long long id);
+cudaError_t btc_sched_plant(unsigned long long id);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -97,6 +94,15 @@ bool gemm_tc_supported(int64_t P, int Kt, int Nt);
 int dx_tensor_core(const void* dy, const void* W, void* dX, int B, int Cout, int CK, int64_t P,
                    cudaStream_t st, const int* rows_of_channels = nullptr, bool f16 = false);
 cudaError_t gemm_status(int32_t* v, bool clear);
+
+// Words of failed range checks, one per unit (disco_bounds.cuh): OR into *v
+// and optionally clear; always 0 outside the bounds-checked build.
+cudaError_t contract_bounds(int32_t* v, bool clear);
+cudaError_t psi_bounds(int32_t* v, bool clear);
+cudaError_t tc_bounds(int32_t* v, bool clear);
+cudaError_t btc_bounds(int32_t* v, bool clear);
+cudaError_t gemm_bounds(int32_t* v, bool clear);
+cudaError_t fused_bounds(int32_t* v, bool clear);
 // Weight gradient dW[o][j] = sum_b sum_p dy[b][o][p] X[b][j][p] (split reduction
 // through fp32 partials of dw_partial_bytes bytes, then rounded to bf16).
 bool dw_tensor_core_supported(int B, int Cout, int CK, int64_t P);

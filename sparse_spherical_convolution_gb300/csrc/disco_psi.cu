@@ -35,6 +35,7 @@
 
 #include <vector>
 
+#include "disco_bounds.cuh"
 #include "disco_internal.cuh"
 
 namespace disco {
@@ -308,6 +309,9 @@ struct PsiOut {
   uint16_t* gtab;
   uint16_t* ftab_h;  // the same tables rounded to fp16
   uint16_t* gtab_h;
+  // element counts the plan sized the arrays for (extent checks of the
+  // bounds-checked build)
+  long long nnz, nnz_csr, nruns, nhval, nftab, ngrp_ent, ngtab;
 };
 
 __device__ __forceinline__ int ring_of(int kind, int k) { return kind == 1 ? k / 3 : k; }
@@ -400,7 +404,8 @@ __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     run.len = len;
     run.npair = npair;
     run.anti = anti;
-    p.runs[ws.runidx[t]] = run;
+    if (DISCO_IN_BOUNDS(ws.runidx[t] >= 0 && ws.runidx[t] < p.nruns)) p.runs[ws.runidx[t]] = run;
+    if (!DISCO_IN_BOUNDS(e0 >= 0 && (long long)e0 + len <= p.nnz)) continue;
     int32_t rpos[kMaxRad];
     for (int r = 0; r < g.R; ++r) rpos[r] = ws.csroff[t * g.R + r];
     for (int j = 0; j < len; ++j) {
@@ -427,8 +432,10 @@ __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
         p.val[e * g.Kp + k] = vals[k];
         if (st[r]) {
           int32_t pos = p.csr_row_ptr[k * g.Hout + ho] + rpos[r];
-          p.csr_col[pos] = hi * W + wi;
-          p.csr_val[pos] = vals[k];
+          if (DISCO_IN_BOUNDS(pos >= 0 && pos < p.nnz_csr)) {
+            p.csr_col[pos] = hi * W + wi;
+            p.csr_val[pos] = vals[k];
+          }
         }
       }
       for (int k = g.K; k < g.Kp; ++k) p.val[e * g.Kp + k] = 0.f;
@@ -444,7 +451,7 @@ __global__ void fill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
         hrow = hoff + npair + 1;
         scale = 0.5f;
       }
-      if (hrow >= 0) {
+      if (hrow >= 0 && DISCO_IN_BOUNDS(hrow < p.nhval)) {
         for (int k = 0; k < g.K; ++k) p.hval[(int64_t)hrow * g.Kp + k] = vals[k] * scale;
         for (int k = g.K; k < g.Kp; ++k) p.hval[(int64_t)hrow * g.Kp + k] = 0.f;
       }
@@ -465,6 +472,10 @@ __global__ void table_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     run_extent(m, g.Win, &dlo, &dhi);
     const int tlf = ftab_len(m, g.Win);
     const int foff = ws.ftofftab[t];
+    // (the whole block reads the same run and skips it alike)
+    if (!DISCO_IN_BOUNDS(r >= 0 && r < p.nruns && foff >= 0 && (long long)foff + g.K * tlf <= p.nftab &&
+                         e0 >= 0 && (long long)e0 + (dhi - dlo + 1) <= p.nnz))
+      continue;
     if (threadIdx.x == 0) p.ftab_off[r] = foff;
     for (int i = threadIdx.x; i < g.K * tlf; i += blockDim.x) {
       const int k = i / tlf, x = i - k * tlf;
@@ -542,7 +553,8 @@ __global__ void gent_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     en.KB = (int16_t)KB;
     en.nch = (int16_t)nch;
     en.pad = 0;
-    p.grp[e++] = en;
+    if (DISCO_IN_BOUNDS(e >= 0 && e < p.ngrp_ent)) p.grp[e] = en;
+    ++e;
     b += g.K * nch;
   });
 }
@@ -552,8 +564,10 @@ __global__ void gfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   const int z = blockIdx.x;
   const int s = g.Win / g.Wout, TQ = grp_tq(s), CW = grp_cw(s), blk = grp_block(s);
   for (int j = p.grp_ptr[z]; j < p.grp_ptr[z + 1]; ++j) {
+    if (!DISCO_IN_BOUNDS(j >= 0 && j < p.ngrp_ent)) break;
     const disco_grp_ent en = p.grp[j];
     const int n = g.K * en.nch * blk;
+    if (!DISCO_IN_BOUNDS(en.off >= 0 && (long long)en.off + n <= p.ngtab && en.ho >= 0 && en.ho < g.Hout)) continue;
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const int bi = i / blk, w = i - bi * blk;  // block (k, c), element (r, ph, y)
       const int k = bi / en.nch, c = bi - k * en.nch;
@@ -568,7 +582,7 @@ __global__ void gfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
         run_extent(m, g.Win, &dlo, &dhi);
         if (m >= 0 && d >= dlo && d <= dhi) {
           const int e0 = p.row_ptr[en.ho] + ws.off[t];
-          v = p.val[(size_t)(e0 + d - dlo) * g.Kp + k];
+          if (DISCO_IN_BOUNDS(e0 + d - dlo >= 0 && e0 + d - dlo < p.nnz)) v = p.val[(size_t)(e0 + d - dlo) * g.Kp + k];
         }
       }
       p.gtab[(size_t)en.off + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -602,7 +616,10 @@ __global__ void tfill_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   int32_t pos = p.trun_ptr[hi];
   for (int ho = 0; ho < g.Hout; ++ho) {
     int32_t r = ws.runidx[(size_t)ho * g.Hin + hi];
-    if (r >= 0) p.truns[pos++] = r;
+    if (r >= 0) {
+      if (DISCO_IN_BOUNDS(pos >= 0 && pos < p.nruns)) p.truns[pos] = r;
+      ++pos;
+    }
   }
 }
 
@@ -616,14 +633,16 @@ __global__ void order_kernel(PsiGeom g, Workspace ws, PsiOut p) {
     int o = ws.rowsum[(size_t)h2 * (kRS + g.R)];
     rank += (o > my) || (o == my && h2 < ho);
   }
-  p.row_order[rank] = ho;
+  if (DISCO_IN_BOUNDS(rank >= 0 && rank < g.Hout)) p.row_order[rank] = ho;
 }
 
 // The page's uniform K-packed form of the union layout; one block per output row.
 __global__ void export_kpacked_kernel(const int32_t* row_ptr, const int32_t* idx, const float* val, int Kp,
                                       int nbr_pad, int64_t* pidx, float* pval, int64_t* pcount) {
   const int ho = blockIdx.x;
-  const int e0 = row_ptr[ho], n = row_ptr[ho + 1] - e0;
+  const int e0 = row_ptr[ho];
+  int n = row_ptr[ho + 1] - e0;
+  if (!DISCO_IN_BOUNDS(n >= 0 && n <= nbr_pad)) n = 0;
   if (threadIdx.x == 0) pcount[ho] = n;
   const int64_t base = (int64_t)ho * nbr_pad;
   for (int j = threadIdx.x; j < nbr_pad; j += blockDim.x) {
@@ -700,11 +719,21 @@ size_t carve_psi(const disco_psi* psi, char* base, PsiOut* out) {
   p.gtab = (uint16_t*)take((size_t)psi->ngtab * 2);
   p.ftab_h = (uint16_t*)take((size_t)psi->nftab * 2);
   p.gtab_h = (uint16_t*)take((size_t)psi->ngtab * 2);
+  p.nnz = psi->nnz;
+  p.nnz_csr = psi->nnz_csr;
+  p.nruns = psi->nruns;
+  p.nhval = psi->nhval;
+  p.nftab = psi->nftab;
+  p.ngrp_ent = psi->ngrp_ent;
+  p.ngtab = psi->ngtab;
   if (out) *out = p;
   return o;
 }
 
 }  // namespace
+// This unit's word of failed range checks (always 0 outside the bounds-checked build).
+DISCO_BOUNDS_READER(psi_bounds)
+
 }  // namespace disco
 
 using namespace disco;

@@ -11,15 +11,30 @@
 //
 // The counter must be private to one launch, also when several launches run
 // at once on different streams, and the library allocates no memory.  So
-// each kernel family owns a file-scope table of slots; a launch carries a
-// process-unique id (next_launch_id) and uses slot id % kSchedSlots:
-//   claim    one thread per CTA swaps the slot's owner from 0 to the id (or
-//            finds the id already there, set by a sibling CTA); a slot still
-//            held by an earlier launch is waited for, with a bound;
-//   next     atomicAdd on the slot's counter;
-//   release  the CTA that finishes last resets the counters and frees the
-//            slot.
-// A claim that times out reports failure: the CTA then takes no tile.
+// each kernel family owns a file-scope table of 64-bit words; a launch
+// carries a process-unique id (next_launch_id) and uses word id % kSchedSlots:
+//
+//   bits 63..34  tag: the low 30 bits of the id of the launch using the word
+//   bits 33..24  active: CTAs of that launch that joined and have not left
+//   bits 23..0   next tile to hand out
+//
+//   join   (once per CTA, compare-and-swap) if the tag is the launch's own,
+//          active + 1; if another launch's tag is there with no active CTA,
+//          take the word: own tag, active 1, counter 0; otherwise another
+//          launch is still drawing: wait, bounded, and give up (the CTA then
+//          takes no tile and flags its status bit);
+//   next   atomicAdd of 1 (only between a CTA's join and its leave);
+//   leave  (once per joined CTA, on every exit path) active - 1.
+//
+// Only joined CTAs count in `active` and every joined CTA leaves, so once
+// all CTAs of a launch have exited its word has no active CTA and the next
+// launch that maps to it takes it over: no failure leaves a word held.
+// While a CTA draws, its launch's active count is non-zero, so no other
+// launch can take the word: every draw lands on the drawing launch's own
+// counter.  A CTA that gives up waiting loses no tile (its siblings draw
+// them all); a CTA that joins late, after its launch's word was taken over
+// and freed, takes it back and recomputes its launch's tiles, whose outputs
+// are plain stores of values that depend on the inputs alone.
 #pragma once
 
 #include <stdint.h>
@@ -27,37 +42,54 @@
 namespace disco {
 
 constexpr int kSchedSlots = 1024;
+constexpr unsigned long long kSchedCountMask = (1ull << 24) - 1;
+constexpr unsigned long long kSchedActiveOne = 1ull << 24;
+constexpr unsigned long long kSchedActiveMask = ((1ull << 10) - 1) << 24;
+constexpr unsigned long long kSchedTagMask = ~(kSchedCountMask | kSchedActiveMask);
+constexpr int kSchedMaxCtas = (1 << 10) - 1;  // CTAs of one launch (active field)
 
-struct SchedSlot {
-  unsigned long long owner;  // launch id holding the slot, 0 = free
-  int next;                  // next tile to hand out
-  int done;                  // CTAs of the owner that finished
-};
+__host__ __device__ __forceinline__ unsigned long long sched_tag(unsigned long long id) {
+  return (id & ((1ull << 30) - 1)) << 34;
+}
 
-__device__ __forceinline__ SchedSlot* sched_claim(SchedSlot* table, unsigned long long id, uint32_t limit) {
-  SchedSlot* s = table + (id % kSchedSlots);
+// Joins the launch's word; nullptr if another launch kept drawing from it for
+// `limit` polls.  One thread per CTA.
+__device__ __forceinline__ unsigned long long* sched_join(unsigned long long* table, unsigned long long id,
+                                                          uint32_t limit) {
+  unsigned long long* w = table + (id % kSchedSlots);
+  const unsigned long long tag = sched_tag(id);
+  unsigned long long old = *(volatile unsigned long long*)w;
   for (uint32_t i = 0; i < limit; ++i) {
-    const unsigned long long o = atomicCAS(&s->owner, 0ull, id);
-    if (o == 0ull || o == id) {
-      __threadfence();
-      return s;
+    unsigned long long want;
+    if ((old & kSchedTagMask) == tag) {
+      want = old + kSchedActiveOne;
+    } else if ((old & kSchedActiveMask) == 0) {
+      want = tag | kSchedActiveOne;
+    } else {
+      __nanosleep(200);
+      old = *(volatile unsigned long long*)w;
+      continue;
     }
-    __nanosleep(200);
+    const unsigned long long seen = atomicCAS(w, old, want);
+    if (seen == old) {
+      __threadfence();
+      return w;
+    }
+    old = seen;
   }
   return nullptr;
 }
 
-__device__ __forceinline__ int sched_next(SchedSlot* s) { return atomicAdd(&s->next, 1); }
+// Next tile of the launch (values past its tile count: none left).  The
+// launch keeps tiles + CTAs below 2^24 (checked on the host).
+__device__ __forceinline__ int sched_next(unsigned long long* w) {
+  return (int)(atomicAdd(w, 1ull) & kSchedCountMask);
+}
 
-// Called once per CTA that claimed the slot, after its last sched_next.
-__device__ __forceinline__ void sched_release(SchedSlot* s) {
+// Once per joined CTA, after its last sched_next.
+__device__ __forceinline__ void sched_leave(unsigned long long* w) {
   __threadfence();
-  if (atomicAdd(&s->done, 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1) {
-    atomicExch(&s->next, 0);
-    atomicExch(&s->done, 0);
-    __threadfence();
-    atomicExch(&s->owner, 0ull);
-  }
+  atomicAdd(w, 0ull - kSchedActiveOne);
 }
 
 }  // namespace disco

@@ -49,11 +49,10 @@ def test_wait_check_rejects_bad_limits(lib):
         assert e.value.status == -1
 
 
-def _held_slot_case(lib, fwd: bool):
-    """A scheduler slot left held (as a launch that failed part-way could
-    leave it): the next persistent launch gives up after its bounded wait,
-    computes nothing and flags the status word; clearing the status frees the
-    slot and the launch after that is correct."""
+def _foreign_tag_case(lib, fwd: bool):
+    """The scheduler word of the next persistent launch holds another
+    launch's tag with its counter part-way (as every earlier launch leaves
+    it): the launch takes the word over and computes every tile."""
     gi = go = (64, 128, 0)
     ref = oracle.build_psi(gi, go, 0, 5, 3 * math.pi / 64)
     psi = lib.Psi(gi, go, 0, 5, 3 * math.pi / 64)
@@ -63,15 +62,9 @@ def _held_slot_case(lib, fwd: bool):
     G = torch.randn((B, C, ref.K, 64, 128), generator=g).to(torch.bfloat16).cuda()
     inp, shape = (x, (B, C, ref.K, 64, 128)) if fwd else (G, (B, C, 64, 128))
     call = lib.disco_fwd if fwd else lib.disco_bwd
-    bit = 4 if fwd else 8
     assert lib.disco_device_status(clear=True) == 0
     out = torch.full(shape, 3.0, dtype=torch.bfloat16, device="cuda")
-    lib.disco_check_sched_hold()
-    call(psi.c, inp, out, B, C)
-    assert lib.disco_device_status(clear=False) & bit
-    assert torch.all(out == 3.0)            # no tile was taken
-    assert lib.disco_device_status(clear=True) & bit   # read, then cleared: the slot is free again
-    out.fill_(3.0)
+    lib.disco_check_sched_takeover()   # also walks the protocol on a private word
     call(psi.c, inp, out, B, C)
     assert lib.disco_device_status() == 0
     if fwd:
@@ -79,11 +72,15 @@ def _held_slot_case(lib, fwd: bool):
     else:
         want, S = oracle.bwd(ref, to_np32(G))
     assert rel_err(to_np32(out), want, S) <= TOL[torch.bfloat16]
+    out2 = torch.full(shape, 3.0, dtype=torch.bfloat16, device="cuda")
+    call(psi.c, inp, out2, B, C)   # the launch after it draws from its own word as usual
+    assert lib.disco_device_status() == 0
+    assert torch.equal(out, out2)
 
 
-def test_held_scheduler_slot_is_recovered_forward(lib):
-    _held_slot_case(lib, True)
+def test_foreign_scheduler_tag_is_taken_over_forward(lib):
+    _foreign_tag_case(lib, True)
 
 
-def test_held_scheduler_slot_is_recovered_transpose(lib):
-    _held_slot_case(lib, False)
+def test_foreign_scheduler_tag_is_taken_over_transpose(lib):
+    _foreign_tag_case(lib, False)
