@@ -38,12 +38,15 @@
 // the pipeline runs across tile boundaries:
 //   warp 0      producer: per tile the tile index and the group's entry list
 //               (bulk copy) into one of two info slots, per item (ho, k,
-//               chunk) the psi block (bulk copy) and 1-2 G boxes (TMA);
+//               chunk) i with i % 3 == 0 the psi block (bulk copy) and 1-2 G
+//               boxes (TMA);
 //   warp 1      MMA issuer (one thread);
 //   warps 2-7   build T;
 //   warps 8-11  epilogue: tcgen05.ld, bf16, TMA stores;
-//   warp 12     second producer: the odd items' copies (one thread issuing
-//               all 16 KB boxes caps the load rate near 35 GB/s per SM).
+//   warps 12-13 the other producers: the copies of items i % 3 == 1, 2 (one
+//               thread issuing all 16 KB boxes caps the load rate near 35
+//               GB/s per SM; the boxes of G in rows of channels, rows W_out
+//               apart, go faster the more threads issue them).
 // All mbarrier waits are bounded (time-out -> status flag, abort).
 
 #include <cudaTypedefs.h>
@@ -60,13 +63,17 @@ __device__ unsigned long long g_btc_sched[kSchedSlots];
 
 namespace {
 
-constexpr int kThreads = 416;
+constexpr int kProducers = 3;               // warp 0 issues items i % 3 == 0, warps 12, 13 the others
+constexpr int kThreads = 384 + 32 * (kProducers - 1);
 constexpr int kBuilderThreads = 192;        // warps 2-7
 constexpr int kEpiThreads = 128;            // warps 8-11
-constexpr int kProducers = 2;               // warps 0 and 12 issue the even / odd items' copies
 constexpr int kN = 256;                     // MMA N = 8 rows x 32 columns
 constexpr int kNT = 2;                      // column blocks per tile
 constexpr int kStages = 3;
+// a producer waits on the stage of its own previous item: the ring must be at
+// least as deep as the producers' item stride, or it would wait on a phase of
+// another producer's item
+static_assert(kStages >= kProducers, "one stage per producer at least");
 constexpr int kMaxEnt = 128;                // entries (output rows) of one group
 constexpr uint32_t kBoxBytes = 128 * 128;   // 128 channels x 64 columns bf16
 constexpr uint32_t kNarrowBytes = 128 * 16; // 128 channels x 8 columns
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tslot;
 
   // Copies of item i (stage i % kStages): the psi block and the 1-2 G boxes.
-  // Issued by producer i & 1 after the stage's previous MMAs completed.
+  // Issued by producer i % kProducers after the stage's previous MMAs completed.
   auto issue_item = [&](int i, const disco_grp_ent& en, int k, int c, int qb, int bc0) -> bool {
     const int s = i % kStages;
     if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag)
@@ -252,15 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // after a failure: let this producer's copies in flight land before the CTA
   // exits (n = one past its last issued item)
   auto drain_own = [&](int n, int who) {
-    for (int li = n - 1; li >= 0 && li >= n - 2 * kStages; --li)
-      if ((li & 1) == who) {
+    for (int li = n - 1; li >= 0 && li >= n - kProducers * kStages; --li)
+      if (li % kProducers == who) {
         mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
         mbar_wait(&fullT[li % kStages], (li / kStages) & 1, kWaitLimit);
       }
   };
 
   if (warp == 0) {
-    // ------------------------------------------- producer (even items) --
+    // ------------------------------------------- producer (items i % 3 == 0) --
     if (lane == 0) {
       int i = 0, tl = 0, done = 0;  // done: one past the last item this thread issued
       bool ok = true;
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const disco_grp_ent en = info[j];
           for (int k = 0; k < a.K && ok; ++k)
             for (int c = 0; c < en.nch && ok; ++c, ++i)
-              if ((i & 1) == 0 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
+              if (i % kProducers == 0 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
         }
       }
       if (!ok) {
@@ -431,8 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       btc_flag(kStatusBtcTimeout);
       *abort_flag = 1;
     }
-  } else if (warp == 12) {
-    // -------------------------------------------- producer (odd items) --
+  } else if (warp >= 12) {
+    // ----------------------------------- producers of items i % 3 == 1, 2 --
+    const int who = warp - 11;
     if (lane == 0) {
       int i = 0, done = 0;
       bool ok = true;
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const disco_grp_ent en = info[j];
           for (int k = 0; k < a.K && ok; ++k)
             for (int c = 0; c < en.nch && ok; ++c, ++i)
-              if ((i & 1) == 1 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
+              if (i % kProducers == who && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
         }
         if (!ok) break;
         mbar_arrive(&info_empty[b]);
@@ -460,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
-        drain_own(done, 1);
+        drain_own(done, who);
       }
     }
   } else {

@@ -36,8 +36,14 @@ __device__ int g_gemm_status = 0;
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;           // dw_gemm_kernel: producer, MMA, 4 epilogue warps
 constexpr int kEpiThreads = 128;
+// gemm_tc_kernel: producer, MMA and 8 epilogue warps, two per TMEM lane
+// quadrant, taking alternate 16-output steps (its epilogue, not the MMA,
+// bounds the dX GEMM, whose tiles have a short reduction)
+constexpr int kGEpiWarps = 8;
+constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGEpiThreads = 32 * kGEpiWarps;
 constexpr int kBM = 128;                  // pixels per tile
 constexpr int kBK = 64;                   // j per stage
 constexpr int kStages = 4;
@@ -45,7 +51,7 @@ constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB: two 64-pixel boxes
 constexpr uint32_t kBMax = 256 * kBK * 2;     // 32 KB: up to 256 outputs
 constexpr uint32_t kStageBytes = kABytes + kBMax;
 constexpr uint32_t kEpiStage = 16 * 32 * 2;      // per epilogue warp: 16 outputs x 32 pixels bf16
-constexpr size_t kSmem = (size_t)kStages * kStageBytes + 4 * kEpiStage + 256 + 1024;
+constexpr size_t kSmem = (size_t)kStages * kStageBytes + kGEpiWarps * kEpiStage + 256 + 1024;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr int kStatusGemmTimeout = 2;
 
@@ -105,13 +111,13 @@ struct GemmTcArgs {
 };
 
 template <bool kBMN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                    const GemmTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint16_t* epi_stage = reinterpret_cast<uint16_t*>(smem + kStages * kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 4 * kEpiStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + kGEpiWarps * kEpiStage);
   uint64_t* full = bars;                   // [kStages]
   uint64_t* empty = bars + kStages;        // [kStages]
   uint64_t* accf = bars + 2 * kStages;     // [2] accumulator complete (commit)
@@ -131,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], kEpiThreads);
+      mbar_init(&acce[b], kGEpiThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -239,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------- epilogue (warps 2-5) --
-    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+    // ------------------------------------------------- epilogue (warps 2-9) --
+    const int q = warp & 3;             // TMEM lanes 32q .. 32q+31
+    const int half = (warp - 2) >> 2;   // output steps c0 = 16 half + 32 j
     int tl = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
       const int ab = tl & 1;
@@ -269,16 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t pp = pw + (lane & 3) * 8;
         rho = pp / a.ctW;
         rwo = pp - rho * a.ctW;
-        dc = 16 / a.ctK;
-        dk = 16 - dc * a.ctK;
+        dc = 32 / a.ctK;
+        dk = 32 - dc * a.ctK;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int n = n0 + (lane >> 2) + 8 * h;
+          const int n = n0 + 16 * half + (lane >> 2) + 8 * h;
           rc[h] = n / a.ctK;
           rk[h] = n - rc[h] * a.ctK;
         }
       }
-      for (int c0 = 0; c0 < a.NB; c0 += 16) {
+      for (int c0 = 16 * half; c0 < a.NB; c0 += 32) {
         float v[16];
         tmem_ld16(tmem + ab * 256 + ((uint32_t)(q * 32) << 16) + c0, v);
 #pragma unroll
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // next step: n += 16
+        for (int h = 0; h < 2; ++h) {  // next step: n += 32
           rc[h] += dc;
           rk[h] += dk;
           if (rk[h] >= a.ctK) {
@@ -607,7 +614,7 @@ int launch_gemm(const void* A, const void* W, void* out, int B, int Kt, int Nt, 
   const long long ntiles = (long long)g.mt * g.nt * B;
   if (ntiles > 0x7fffffffLL) return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
   const int grid = (int)(ntiles < sm_count_g() ? ntiles : sm_count_g());
-  kern<<<grid, kThreads, kSmem, st>>>(amap, bmap, g);
+  kern<<<grid, kGThreads, kSmem, st>>>(amap, bmap, g);
   return check_launch("tensor-core GEMM");
 }
 
