@@ -34,6 +34,20 @@ def test_exports_every_declared_symbol(lib):
     assert set(declared) == set(lib.EXPORTED_SYMBOLS)
 
 
+def test_bounds_checked_build_exports_the_same_symbols(lib):
+    """The bounds-checked build (-DDISCO_DEBUG_BOUNDS) compiles from the same
+    sources, exports the same symbols and says which build it is."""
+    from sparse_spherical_convolution_gb300 import build
+    path = build.build(debug_bounds=True)
+    assert path == build.LIB_BOUNDS and path != build.LIB
+    so = ctypes.CDLL(path)
+    for name in _declared_functions():
+        assert hasattr(so, name), name
+    so.disco_build_flags.restype = ctypes.c_int32
+    assert so.disco_build_flags() == lib.DISCO_BUILD_DEBUG_BOUNDS
+    assert lib.disco_build_flags() == 0
+
+
 def test_version_and_error_string(lib):
     assert lib.disco_version() >= 100
     assert isinstance(lib.disco_last_error(), str)
