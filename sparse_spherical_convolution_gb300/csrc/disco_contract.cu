@@ -1,8 +1,9 @@
 // disco_contract.cu -- forward and transpose DISCO contractions on CUDA cores.
 //
 // DISCO Kernel Development Guide (torch-harmonics):
-//  * §Architecture snapshot: forward = CSR sparse contraction inp -> (B,C,K,H,W),
-//    backward = CSR transpose contraction (B,C,K,H,W) -> inp.
+//  * §Architecture snapshot: the forward kernel contracts the input grid with
+//    the sparse psi into the [B, C, K, H_out, W_out] tensor; the backward
+//    kernel applies the transpose of that map, back to the input grid.
 //  * §Backward direction: both run in the gather direction (each output
 //    element reads a bounded neighbourhood), with no atomics; the scatter
 //    backward was retired because of atomic contention.
