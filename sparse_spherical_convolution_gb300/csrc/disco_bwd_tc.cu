@@ -417,15 +417,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* T = st + 2 * kBoxBytes;
             const uint16_t* tab = reinterpret_cast<const uint16_t*>(st + 2 * kBoxBytes + kTBytes);
             const int nq = 2 * min(4, KB - 4 * c);  // 16-byte chunks per T row
-            for (int idx = btid; idx < kN * nq; idx += kBuilderThreads) {
-              const int n = idx & (kN - 1), q8 = idx >> 8;
-              const int r = n >> 5, rem = n & 31;
-              const int t = rem / S, p = rem - t * S;
-              const uint16_t* src = tab + (r * S + p) * CW + 8 * q8 - t + TQ - 1;
-              uint32_t w[4];
+            // T[(r, t, p), 8 q8 + e] = tab[r][p][8 q8 + TQ - 1 - t + e]: the rows
+            // t = 8 g + j (j = 0..7) of one (r, p, q8) read the same 16 table
+            // values from the aligned index 8 q8 + TQ - 8 - 8 g on, shifted by
+            // 7 - j.  One unit (r, p, g, q8) loads them with two 16-byte loads
+            // and writes the 8 rows' chunks q8; q8 varies fastest across lanes
+            // (conflict-free loads, and stores that cover all banks)
+            constexpr int kG = TQ / 8;  // row groups of 8 t per (r, p)
+            for (int u = btid; u < 8 * S * kG * nq; u += kBuilderThreads) {
+              const int q8 = u % nq, rest = u / nq;
+              const int g = rest % kG, rp = rest / kG;  // rp = r S + p
+              const int r = rp / S, p = rp - r * S;
+              const uint4* src = reinterpret_cast<const uint4*>(tab + rp * CW + 8 * (q8 + kG - 1 - g));
+              const uint4 lo = src[0], hi = src[1];
+              const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) w[e] = (uint32_t)src[2 * e] | ((uint32_t)src[2 * e + 1] << 16);
-              *reinterpret_cast<uint4*>(T + n * 128 + ((q8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int j = 0; j < 8; ++j) {
+                const int m = 7 - j;  // first of the row's 8 values among the 16 loaded
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  w[e] = (m & 1) ? __funnelshift_r(v[m / 2 + e], v[m / 2 + e + 1], 16) : v[m / 2 + e];
+                const int n = r * 32 + (8 * g + j) * S + p;
+                *reinterpret_cast<uint4*>(T + n * 128 + ((q8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
             fence_proxy_async_smem();
             mbar_arrive(&fullB[s]);
