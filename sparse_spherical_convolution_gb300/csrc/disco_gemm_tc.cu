@@ -21,7 +21,9 @@
 // main loop of the next:
 //   warp 0  TMA producer (one thread),
 //   warp 1  MMA issuer (one thread, TMEM owner),
-//   warps 2-5 epilogue: tcgen05.ld, bf16, stores coalesced along pixels.
+//   warps 2-9 epilogue: tcgen05.ld, bf16, stores coalesced along pixels
+//            (two warps per TMEM lane quadrant, alternate 16-output steps).
+// The dW kernel below keeps four epilogue warps (warps 2-5).
 // All mbarrier waits are bounded (time-out -> status flag, abort).
 
 #include <cudaTypedefs.h>
