@@ -338,6 +338,20 @@ def run_ours(args):
     # tensor rate inside the fused call (its flops over the whole call's time:
     # a lower bound on the einsum's own rate) against the sustained bf16 peak
     tc_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # useful flops of the contractions (CSR non-zeros only) against what the
+    # FP32 CUDA cores could do at most: SMs x 128 FP32 lanes x 2 flop x clock.
+    # Above 1 means beyond the bound of a CUDA-core gather (the tensor-core
+    # Toeplitz tiles run 5-10x the useful flops).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    fp32_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+    contraction_flops = {"useful_flops_per_call": alg["csr_flops"],
+                         "fp32_alu_peak_tflops": round(fp32_peak, 1),
+                         "fp32_alu_peak_derivation": f"{sms} SMs x 128 FP32 lanes x 2 flop x {sm_mhz:.0f} MHz"}
+    for nm in ("fwd", "bwd"):
+        tf = alg["csr_flops"] / (med[nm] * 1e-3) / 1e12
+        contraction_flops[nm + "_tflops"] = round(tf, 1)
+        contraction_flops[nm + "_frac_of_fp32_alu"] = round(tf / fp32_peak, 3)
     fused_calls = None
     if "fused_bytes" in alg:
         ein_tf = alg["einsum_flops"] / (med["fused"] * 1e-3) / 1e12
@@ -382,6 +396,7 @@ def run_ours(args):
                                        "algorithmic_bytes_per_launch": alg[other + "_bytes"],
                                        "ms_per_launch": round(med[other], 3)},
         "fused_calls": fused_calls,
+        "contraction_flops": contraction_flops,
         "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": peak_src,
         "clocks": clocks, "gpu_launches": launches_per_step * args.steps, "e2e": e2e,
     }
