@@ -137,6 +137,65 @@ __device__ __forceinline__ RunGeom run_geom(const disco_run& r, int Win) {
   return g;
 }
 
+// Builder of one K-chunk of T (the B operand, [16 K rows (k, t)] x [64 window
+// columns], 128-byte swizzled): T[(k, t), 8 gi + e] = tab[k][x0 + e] with
+// x0 = off + 8 gi - S t, zero where x0 + e lies outside the run's table row
+// [0, TL) (the table holds psi_k of offset delta at index 8 + delta - dlo,
+// so off = 8 + 64 c - M - dlo for chunk c).  The rows t = 8 g + j
+// (j = 0..7) of one (k, gi) read one stretch of the table row starting at
+// lo = off + 8 gi - 8 S g - 7 S; lo mod 8 (sh) is the same for the whole run,
+// so one unit (k, g, gi) loads the stretch as four aligned 16-byte blocks
+// (each wholly inside or outside [0, TL), both multiples of 8) and writes its
+// 8 rows with shifts known at compile time, in one of 8 variants picked by
+// sh.  gi varies fastest across threads: conflict-free loads and stores.
+template <int S, int SH>
+__device__ __forceinline__ void t_rows(const uint32_t (&v)[16], uint8_t* sB, int n0, int gi) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int m = SH + S * (7 - j);  // first value of row j within the stretch
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (m & 1) ? __funnelshift_r(v[m / 2 + e], v[m / 2 + e + 1], 16) : v[m / 2 + e];
+    const int n = n0 + j;
+    *reinterpret_cast<uint4*>(sB + n * 128 + ((gi ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int K, int S>
+__device__ __forceinline__ void build_t_chunk(const uint16_t* tab, int TL, int off, int ngrp, uint8_t* sB,
+                                              int btid, int nthreads) {
+  const int sh = (off - 7 * S) & 7;
+  for (int u = btid; u < K * 2 * ngrp; u += nthreads) {
+    const int gi = u % ngrp, kg = u / ngrp;  // kg = 2 k + g
+    const int k = kg >> 1, g = kg & 1;
+    const int lo = off + 8 * gi - 8 * S * g - 7 * S;
+    const int A = lo - sh;  // multiple of 8
+    const uint16_t* row = tab + (size_t)k * TL;
+    uint32_t v[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int x = A + 8 * q;
+      const uint4 b = (x >= 0 && x < TL) ? *reinterpret_cast<const uint4*>(row + x) : make_uint4(0u, 0u, 0u, 0u);
+      v[4 * q] = b.x;
+      v[4 * q + 1] = b.y;
+      v[4 * q + 2] = b.z;
+      v[4 * q + 3] = b.w;
+    }
+    const int n0 = k * 16 + 8 * g;
+    switch (sh) {  // the same in every thread
+      case 0: t_rows<S, 0>(v, sB, n0, gi); break;
+      case 1: t_rows<S, 1>(v, sB, n0, gi); break;
+      case 2: t_rows<S, 2>(v, sB, n0, gi); break;
+      case 3: t_rows<S, 3>(v, sB, n0, gi); break;
+      case 4: t_rows<S, 4>(v, sB, n0, gi); break;
+      case 5: t_rows<S, 5>(v, sB, n0, gi); break;
+      case 6: t_rows<S, 6>(v, sB, n0, gi); break;
+      default: t_rows<S, 7>(v, sB, n0, gi); break;
+    }
+  }
+}
+
 template <int K, int S, int STAGES>
 struct TcCfg {
   static constexpr int N = 16 * K;                           // MMA N
@@ -361,26 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* sB = smem + s * Cfg::kStageBytes + Cfg::kABytes;
         const int nks = min(kCK, g.KS - c * kCK);
         const int ngrp = 2 * nks;  // 8-column groups of this chunk
-        for (int idx = btid; idx < N * ngrp; idx += kBuilderThreads) {
-          const int n = idx % N, gi = idx / N;
-          const int k = n >> 4, t = n & 15;
-          // table index of the first of the 8 consecutive offsets of this group
-          const int x0 = 8 + c * kChunkCols + 8 * gi - S * t - g.M - g.dlo;
-          uint32_t w[4] = {0u, 0u, 0u, 0u};
-          if (x0 + 7 >= 0 && x0 < g.TL) {
-            const uint16_t* row = tab + (size_t)k * g.TL;
-            uint16_t v[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int x = x0 + e;
-              v[e] = (x >= 0 && x < g.TL) ? row[x] : (uint16_t)0;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = (uint32_t)v[2 * e] | ((uint32_t)v[2 * e + 1] << 16);
-          }
-          *reinterpret_cast<uint4*>(sB + n * 128 + ((gi ^ (n & 7)) << 4)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        build_t_chunk<K, S>(tab, g.TL, 8 + c * kChunkCols - g.M - g.dlo, ngrp, sB, btid, kBuilderThreads);
         fence_proxy_async_smem();
         mbar_arrive(&fullB[s]);
       }
@@ -771,24 +811,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           uint8_t* sB = smem + s * Cfg::kStageBytes + Cfg::kABytes;
           const int nks = min(kCK, g.KS - c * kCK);
           const int ngrp = 2 * nks;
-          for (int idx = btid; idx < N * ngrp; idx += kBuilderThreads) {
-            const int n = idx % N, gi = idx / N;
-            const int k = n >> 4, tt = n & 15;
-            const int x0 = 8 + c * kChunkCols + 8 * gi - S * tt - g.M - g.dlo;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
-            if (x0 + 7 >= 0 && x0 < g.TL) {
-              const uint16_t* row = tab + (size_t)k * g.TL;
-              uint16_t v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int x = x0 + e;
-                v[e] = (x >= 0 && x < g.TL) ? row[x] : (uint16_t)0;
-              }
-#pragma unroll
-              for (int e = 0; e < 4; ++e) w[e] = (uint32_t)v[2 * e] | ((uint32_t)v[2 * e + 1] << 16);
-            }
-            *reinterpret_cast<uint4*>(sB + n * 128 + ((gi ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          build_t_chunk<K, S>(tab, g.TL, 8 + c * kChunkCols - g.M - g.dlo, ngrp, sB, btid, kBuilderThreads);
           fence_proxy_async_smem();
           mbar_arrive(&fullB[s]);
         }
