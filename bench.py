@@ -30,6 +30,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOAD = "down_fused_bwd_721x1440_to_361x720"
+# the oracle arm's warm-up and timed steps together take about this long
+REF_TOTAL_S = 150.0
 METRIC = "DISCO fwd/bwd contraction HBM GB/s (% of peak); fused conv ms/call"
 
 
@@ -427,12 +429,33 @@ def _traffic_from_profiles(kernel: str, workload: str):
         return None
 
 
-def cpu_baseline(w, budget_s: float, ref=None):
+def _psi_rows(ref, m: int):
+    """The oracle's psi restricted to every m-th output row (all k): a sample
+    of the output rows, spread over all latitudes (the polar rows cost more).
+    Only the CSR arrays, which the oracle's contractions read, are sliced;
+    the oracle computes on them as it stands."""
+    import dataclasses
+    import numpy as np
+    if m <= 1:
+        return ref, 1.0
+    rows = np.arange(0, ref.Hout, m)
+    starts = np.array([ref.csr_row_ptr[k * ref.Hout + h] for k in range(ref.K) for h in rows], np.int64)
+    ends = np.array([ref.csr_row_ptr[k * ref.Hout + h + 1] for k in range(ref.K) for h in rows], np.int64)
+    ptr = np.concatenate([[0], np.cumsum(ends - starts)]).astype(np.int64)
+    sel = np.concatenate([np.arange(a, b) for a, b in zip(starts, ends)]) if len(starts) else np.zeros(0, np.int64)
+    sub = dataclasses.replace(ref, grid_out=(len(rows), ref.grid_out[1], ref.grid_out[2]), csr_row_ptr=ptr,
+                              csr_col=np.ascontiguousarray(ref.csr_col[sel]),
+                              csr_val=np.ascontiguousarray(ref.csr_val[sel]))
+    return sub, len(rows) / ref.Hout
+
+
+def cpu_baseline(w, budget_s: float, ref=None, row_stride: int = 1):
     """The fp64 oracle, as it stands, on a bounded sample of the workload:
     the forward and transpose contractions over the first n channels (n =
-    host cores, one OpenMP thread each), scaled to the same GB/s metric.
-    `ref` is the oracle's psi for the workload (built here when None; the
-    build is init work, outside the timed sample)."""
+    host cores, one OpenMP thread each) and every row_stride-th output row,
+    scaled to the same GB/s metric.  `ref` is the oracle's psi for the
+    workload (built here when None; the build is init work, outside the
+    timed sample)."""
     import numpy as np
     import torch
     import oracle
@@ -440,25 +463,29 @@ def cpu_baseline(w, budget_s: float, ref=None):
     cores = os.cpu_count() or 1
     if ref is None:
         ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
+    sub, rfrac = _psi_rows(ref, row_stride)
     g = torch.Generator().manual_seed(w.seed)
     Hin, Win = w.grid_in[:2]
     Hout, Wout = w.grid_out[:2]
     n = max(1, min(w.C, cores))
     x = torch.randn((1, n, Hin, Win), generator=g).to(torch.bfloat16).double().numpy()
-    G = torch.randn((1, n, w.K, Hout, Wout), generator=g).to(torch.bfloat16).double().numpy()
+    G = torch.randn((1, n, w.K, sub.Hout, Wout), generator=g).to(torch.bfloat16).double().numpy()
     t0 = time.perf_counter()
-    oracle.fwd(ref, x)
+    oracle.fwd(sub, x)
     t1 = time.perf_counter()
-    oracle.bwd(ref, G)
+    oracle.bwd(sub, G)
     t2 = time.perf_counter()
     esz = 2
     frac = n / w.C
-    byts = (x.size + G.size) * esz * 2  # fwd + bwd, input + output, for the sample
+    # fwd + bwd, input + output, for the sampled channels; the sampled rows
+    # carry that fraction of the work
+    byts = (x.size + n * w.K * Hout * Wout) * esz * 2 * rfrac
     del np
+    rows = "all output rows" if row_stride <= 1 else f"every {row_stride}th output row ({rfrac:.3f} of them)"
     return {"value": round(byts / (t2 - t0) / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"fp64 oracle fwd + bwd over {n} of {w.C} channels ({frac:.3f} of the "
-                      f"workload), {t1 - t0:.1f} s + {t2 - t1:.1f} s"}
+                      f"workload) and {rows}, {t1 - t0:.2f} s + {t2 - t1:.2f} s"}
 
 
 def run_reference(args):
@@ -469,12 +496,20 @@ def run_reference(args):
     from sparse_spherical_convolution_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
     ref = oracle.build_psi(w.grid_in, w.grid_out, w.kind, w.nrad, w.cutoff)
+    # every step samples every m-th output row, m chosen from one full-row
+    # step so that the warm-up and timed steps together take about
+    # REF_TOTAL_S (or cpu_budget_s per step, whichever is less)
+    t0 = time.perf_counter()
+    cpu_baseline(w, args.cpu_budget_s, ref)
+    full_s = time.perf_counter() - t0
+    per_step = min(args.cpu_budget_s, REF_TOTAL_S / max(1, args.steps + args.warmup))
+    m = max(1, min(w.grid_out[0], math.ceil(full_s / per_step)))
     vals = []
     cb = None
     for _ in range(args.warmup):
-        cpu_baseline(w, args.cpu_budget_s, ref)
+        cpu_baseline(w, args.cpu_budget_s, ref, m)
     for _ in range(args.steps):
-        cb = cpu_baseline(w, args.cpu_budget_s, ref)
+        cb = cpu_baseline(w, args.cpu_budget_s, ref, m)
         vals.append(cb["value"])
     v = round(statistics.median(vals), 4)
     out = {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
