@@ -38,8 +38,9 @@ __device__ int g_gemm_status = 0;
 
 namespace {
 
-constexpr int kThreads = 192;           // dw_gemm_kernel: producer, MMA, 4 epilogue warps
+constexpr int kThreads = 224;           // dw_gemm_kernel: producer, MMA, 4 epilogue warps, second producer
 constexpr int kEpiThreads = 128;
+constexpr int kDProducers = 2;          // dw_gemm_kernel: warp 0 (items i % 2 == 0) and warp 6 (i % 2 == 1)
 // gemm_tc_kernel: producer, MMA and 8 epilogue warps, two per TMEM lane
 // quadrant, taking alternate 16-output steps (its epilogue, not the MMA,
 // bounds the dX GEMM, whose tiles have a short reduction)
@@ -403,14 +404,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     *q1 = (int)((long long)nq * (*sp + 1) / a.nsplit);
   };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
+    // producers: item i (one reduction step of a tile) by warp 0 when i is
+    // even, by warp 6 when odd; with kStages a multiple of kDProducers a
+    // stage always serves the same producer, which waits only on its own
+    // earlier items (boxes of dy and X rows P apart are issued faster by
+    // two threads than by one)
+    static_assert(kStages % kDProducers == 0, "a stage stays with one producer");
+    const int who = warp == 0 ? 0 : 1;
     if (lane == 0) {
-      int i = 0;
+      int i = 0, done = 0;  // done: one past the last item this thread issued
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         int o0, n0, sp, q0, q1;
         coords(t, &o0, &n0, &sp, &q0, &q1);
         for (int q = q0; q < q1; ++q, ++i) {
+          if (i % kDProducers != who) continue;
           const int s = i % kStages;
           if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag) {
             ok = false;
@@ -428,15 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_complete_tx(&full[s], a.abytes + a.bbytes);
           }
+          done = i + 1;
         }
       }
       if (!ok) {
         gemm_flag();
         *abort_flag = 1;
-        for (int back = 1; back <= kStages && i - back >= 0; ++back) {
-          const int li = i - back;
-          mbar_wait(&full[li % kStages], (li / kStages) & 1, kWaitLimit);
-        }
+        for (int li = done - 1; li >= 0 && li >= done - kDProducers * kStages; --li)
+          if (li % kDProducers == who) mbar_wait(&full[li % kStages], (li / kStages) & 1, kWaitLimit);
       }
     }
   } else if (warp == 1) {
