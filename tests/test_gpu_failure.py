@@ -84,3 +84,35 @@ def test_foreign_scheduler_tag_is_taken_over_forward(lib):
 
 def test_foreign_scheduler_tag_is_taken_over_transpose(lib):
     _foreign_tag_case(lib, False)
+
+
+def test_scheduler_words_reused_across_many_launches(lib):
+    """Many more persistent launches than the scheduler tables have words
+    (1024 per kernel family; launch ids are shared by the families, so
+    alternating forward and transpose launches each reuse every other word),
+    on two streams at once: words are taken over again and again while
+    launches on the other stream draw from theirs.  Every result must equal
+    the one computed alone, bit for bit, with a clean status word."""
+    gi = go = (64, 128, 0)
+    psi = lib.Psi(gi, go, 0, 5, 3 * math.pi / 64)
+    B, C, K = 1, 130, psi.c.K
+    g = torch.Generator(device="cuda").manual_seed(17)
+    x = torch.randn((B, C, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+    G = torch.randn((B, C, K, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+    X0 = torch.empty((B, C, K, 64, 128), dtype=torch.bfloat16, device="cuda")
+    gx0 = torch.empty_like(x)
+    lib.disco_fwd(psi.c, x, X0, B, C)
+    lib.disco_bwd(psi.c, G, gx0, B, C)
+    torch.cuda.synchronize()
+    assert lib.disco_device_status(clear=True) == 0
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    Xs = [torch.empty_like(X0) for _ in range(2)]
+    gxs = [torch.empty_like(gx0) for _ in range(2)]
+    for i in range(1100):  # 2200 persistent launches, alternating streams
+        st = s1 if i % 2 == 0 else s2
+        lib.disco_fwd(psi.c, x, Xs[i % 2], B, C, stream=st)
+        lib.disco_bwd(psi.c, G, gxs[i % 2], B, C, stream=st)
+    torch.cuda.synchronize()
+    assert lib.disco_device_status(clear=True) == 0
+    for X, gx in zip(Xs, gxs):
+        assert torch.equal(X, X0) and torch.equal(gx, gx0)
