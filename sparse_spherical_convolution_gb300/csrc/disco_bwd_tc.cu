@@ -20,33 +20,52 @@
 //   T[(r, t, p), i] = psi_k^{(ho, hi0 + r)}(s (t - i + MW) + p),
 //
 // M = 128 channels, N = 8 rows x 32 columns = 256, K = the window, 16 columns
-// per step.  T does not depend on the block, so one T serves both blocks (the
-// second block reads the G window TQ columns further on).  The T values come
-// from the psi tables by input-row group (disco_psi.gtab), laid out so that a
-// 64-column chunk of T is one contiguous block per (ho, k, chunk): every
-// builder thread reads 8 consecutive values with no bounds logic.
+// per step.  T does not depend on the block, so one T serves both blocks: the
+// second block reads the G window TQ columns (kStep1 = TQ / 16 steps) further
+// on, i.e. window step w meets T step w in block 0 and T step w - kStep1 in
+// block 1.  The T values come from the psi tables by input-row group
+// (disco_psi.gtab), laid out so that a 64-column chunk of T is one contiguous
+// block per (ho, k, chunk): every builder thread reads 8 consecutive values
+// with no bounds logic.
+//
+// One item per 64-column G box of the window: item c of (ho, k) holds box c
+// (window steps 4c .. 4c+3) and T chunk c (T steps 4c .. 4c+3, for block 0
+// and for block 1's steps from 4c on); block 1's first kStep1 steps are T
+// chunk c - 1's last ones, read from the previous item's stage.  So each G
+// box is loaded once per tile, output row and k (pairing both blocks with one
+// window chunk instead would need the next box as well, and load most boxes
+// of a long window twice), and a T chunk is released after the next item's
+// MMAs.
 //
 // Operands are K-major in the 128-byte swizzled layout: the G window arrives
-// by TMA in boxes of 64 columns x 128 channels (a box that would cross the
-// longitude seam is fetched instead as 8 wrapped 8-column boxes in the
-// unswizzled layout and read with that layout's descriptor); T is written in
-// the same swizzled layout by the builder warps.
+// by TMA in boxes of 64 columns x 128 channels; T is written in the same
+// layout by the builder warps.  A window chunk that crosses the longitude
+// seam arrives, for G in the API layout, as two boxes, the chunk's columns
+// before the seam in one and those after it in the other, each zero
+// elsewhere (columns outside the tensor read as zeros), and its MMAs run on
+// both: two 128-row boxes instead of eight 8-column ones, since there a box
+// costs by its rows (each in another channel's pages), not its bytes.  For G
+// in rows of channels, where rows are cheap, it arrives as 8 wrapped 8-column
+// boxes in the unswizzled layout, read with that layout's descriptor.
 //
-// Persistent kernel: one CTA per SM; the producer takes the next tile from
-// the launch's scheduler counter (disco_sched.cuh), in an order that puts the
-// long polar row groups first and keeps the groups that share G rows close;
-// the pipeline runs across tile boundaries:
-//   warp 0      producer: per tile the tile index and the group's entry list
-//               (bulk copy) into one of two info slots, per item (ho, k,
-//               chunk) i with i % 3 == 0 the psi block (bulk copy) and 1-2 G
-//               boxes (TMA);
-//   warp 1      MMA issuer (one thread);
-//   warps 2-7   build T;
-//   warps 8-11  epilogue: tcgen05.ld, bf16, TMA stores;
-//   warps 12-13 the other producers: the copies of items i % 3 == 1, 2 (one
-//               thread issuing all 16 KB boxes caps the load rate near 35
-//               GB/s per SM; the boxes of G in rows of channels, rows W_out
-//               apart, go faster the more threads issue them).
+// Persistent kernel: one CTA per SM; tiles come from the launch's scheduler
+// counter (disco_sched.cuh), in an order that puts the long polar row groups
+// first and keeps the groups that share G rows close; the pipeline runs
+// across tile boundaries.  Rings of 4 G boxes, 4 T chunks and 4 psi blocks;
+// roles:
+//   warp 0      tiles: the tile index and the group's entry list (bulk copy)
+//               into one of two info slots; per item the psi block of its
+//               chunk (bulk copy), up to 4 items ahead of the builders;
+//   warp 1      MMA issuer (one thread; descriptors precomputed per stage);
+//   warps 2, 3, 4, 6, 7, 12  build T into the item's stage;
+//   warps 8-11  epilogue: tcgen05.ld, bf16, TMA stores (warp w reads TMEM
+//               lanes 32 (w % 4) ..);
+//   warps 5, 13 G producers: the box of items i % 2 == 0, 1 (the boxes of G
+//               in rows of channels, rows W_out apart, go faster the more
+//               threads issue them).
+// Warps w and w + 4 share one of the SM's four schedulers: the single-thread
+// MMA issuer and G producers (w % 4 == 1) share theirs with no builder warp.
+// Barriers complete with one arrival per warp (or one commit), not per thread.
 // All mbarrier waits are bounded (time-out -> status flag, abort).
 
 #include <cudaTypedefs.h>
@@ -63,17 +82,18 @@ __device__ unsigned long long g_btc_sched[kSchedSlots];
 
 namespace {
 
-constexpr int kProducers = 3;               // warp 0 issues items i % 3 == 0, warps 12, 13 the others
-constexpr int kThreads = 384 + 32 * (kProducers - 1);
-constexpr int kBuilderThreads = 192;        // warps 2-7
+constexpr int kGProducers = 2;              // warps 5, 13: the G boxes of items i % 2 == 0, 1
+constexpr int kThreads = 384 + 32 * kGProducers;
+constexpr int kBuilderThreads = 192;        // warps 2, 3, 4, 6, 7, 12
 constexpr int kEpiThreads = 128;            // warps 8-11
 constexpr int kN = 256;                     // MMA N = 8 rows x 32 columns
 constexpr int kNT = 2;                      // column blocks per tile
-constexpr int kStages = 3;
-// a producer waits on the stage of its own previous item: the ring must be at
-// least as deep as the producers' item stride, or it would wait on a phase of
-// another producer's item
-static_assert(kStages >= kProducers, "one stage per producer at least");
+constexpr int kTStages = 4;                 // T chunks: built ahead, and kept for the next item
+constexpr int kGStages = 4;                 // G boxes: in flight from L2 or waiting for their MMAs
+constexpr int kTabSlots = 4;                // psi blocks fetched ahead of the builders
+// a G producer waits on the G stage of its own earlier item: every G stage must
+// stay with one producer, or it would wait on a phase of another producer's item
+static_assert(kGStages % kGProducers == 0, "a G stage stays with one G producer");
 constexpr int kMaxEnt = 128;                // entries (output rows) of one group
 constexpr uint32_t kBoxBytes = 128 * 128;   // 128 channels x 64 columns bf16
 constexpr uint32_t kNarrowBytes = 128 * 16; // 128 channels x 8 columns
@@ -136,13 +156,19 @@ template <int S>
 struct BCfg {
   static constexpr int TQ = grp_tq(S);
   static constexpr int CW = grp_cw(S);
-  static constexpr uint32_t kTabBytes = (uint32_t)grp_block(S) * 2;
-  static constexpr uint32_t kTabSlot = (kTabBytes + 1023) & ~1023u;
-  // stage: 2 G box slots | T chunk | psi block
-  static constexpr uint32_t kStageBytes = 2 * kBoxBytes + kTBytes + kTabSlot;
+  static constexpr int kStep1 = TQ / 16;  // K steps between the two blocks' windows (1 or 2)
+  static constexpr uint32_t kTabBytes = (uint32_t)grp_block(S) * 2;  // the psi block of one chunk
+  // layout: T stages | G stages | psi slots | entry lists | gx pieces | barriers
+  static constexpr uint32_t kGOff = kTStages * kTBytes;
+  static constexpr uint32_t kTabOff = kGOff + kGStages * kBoxBytes;
+  static constexpr uint32_t kInfoOff = kTabOff + kTabSlots * kTabBytes;
   static constexpr uint32_t kInfoBytes = 2 * kMaxEnt * sizeof(disco_grp_ent);
+  static constexpr uint32_t kOutOff = kInfoOff + kInfoBytes;
   static constexpr uint32_t kOutBytes = 128 * 32 * 2;  // one gx piece: 128 channels x 32 columns
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kOutBytes + kInfoBytes + 256 + 1024;
+  static constexpr uint32_t kBarOff = kOutOff + 2 * kOutBytes;
+  static constexpr size_t kSmem = (size_t)kBarOff + 512 + 1024;  // + barriers, + alignment slack
+  static_assert(kGOff % 1024 == 0 && kTabBytes % 16 == 0 && kInfoOff % 16 == 0 && kOutOff % 128 == 0,
+                "alignment of the swizzled tiles and copy targets");
 };
 
 // the z-th row group in processing order: poles first, then inwards, so the
@@ -153,59 +179,78 @@ template <int S>
 __device__ __forceinline__ void tile_coords(const BtcArgs& a, int tile, int* qb, int* bc0, int* zg) {
   const int x = tile % a.ntx;
   const int rest = tile / a.ntx;
-  const int y = rest % a.nty;
-  const int z = rest / a.nty;
+  const int z = rest % a.ntz;
+  const int y = rest / a.ntz;
   *qb = x * (kNT * BCfg<S>::TQ);
   *bc0 = y * 128;
   *zg = row_group(z, a.ntz);
 }
 
-// a G box that would cross the longitude seam is fetched as 8 narrow boxes
-__device__ __forceinline__ bool box_is_narrow(int col0, int Wout) { return wrapc(col0, Wout) + 64 > Wout; }
-
+// Items of one entry (output row) and k: one per 64-column G box of the
+// window.  Block 0 reads window steps 0 .. KB-1 and block 1 steps kStep1 ..
+// KB-1+kStep1, so the window spans KB + kStep1 steps of 16 columns.
 template <int S>
+__device__ __forceinline__ int entry_items(const disco_grp_ent& en) {
+  return ((int)en.KB + BCfg<S>::kStep1 + 3) / 4;
+}
+
+// kTwoBox: a window chunk across the longitude seam arrives as two zero-padded
+// 64-column boxes and its MMAs run on both (G in the API layout, where a box
+// costs by its 128 rows, each in another channel's pages); otherwise as 8
+// wrapped 8-column boxes in the unswizzled layout (G in rows of channels,
+// where rows are cheap and the MMAs are not doubled).
+template <int S, bool kTwoBox>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap gwide, const __grid_constant__ CUtensorMap gnarrow,
                   const __grid_constant__ CUtensorMap gxmap, const BtcArgs a) {
   using Cfg = BCfg<S>;
   constexpr int TQ = Cfg::TQ, CW = Cfg::CW;
-  constexpr int kStep1 = TQ / 16;  // K steps between the two blocks' windows
+  constexpr int kStep1 = Cfg::kStep1;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  disco_grp_ent* infos = reinterpret_cast<disco_grp_ent*>(smem + kStages * Cfg::kStageBytes);
-  uint8_t* outbuf = smem + kStages * Cfg::kStageBytes + Cfg::kInfoBytes;  // [2] gx pieces for TMA stores
-  uint64_t* bars = reinterpret_cast<uint64_t*>(outbuf + 2 * Cfg::kOutBytes);
-  uint64_t* fullA = bars;                         // [kStages] G boxes landed
-  uint64_t* fullB = bars + kStages;               // [kStages] T built (192 arrivals)
-  uint64_t* empty = bars + 2 * kStages;           // [kStages] MMAs of the stage done (commit)
-  uint64_t* info_full = bars + 3 * kStages;       // [2] entry list landed
-  uint64_t* info_empty = bars + 3 * kStages + 2;  // [2] entry list released by all readers
-  uint64_t* acc_full = bars + 3 * kStages + 4;    // all MMAs of a tile done (commit)
-  uint64_t* tmem_empty = bars + 3 * kStages + 5;  // epilogue read TMEM out (128 arrivals)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 6);
-  int32_t* info_cnt = reinterpret_cast<int32_t*>(bars + 3 * kStages + 7);  // [2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kStages + 8);
-  volatile int* tile_id = reinterpret_cast<volatile int*>(bars + 3 * kStages + 9);  // [2], -1 = no more tiles
-  // [kStages] psi block landed: the builders start T while the G boxes are still in flight
-  uint64_t* fullT = bars + 3 * kStages + 10;
+  disco_grp_ent* infos = reinterpret_cast<disco_grp_ent*>(smem + Cfg::kInfoOff);
+  uint8_t* outbuf = smem + Cfg::kOutOff;  // [2] gx pieces for TMA stores
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  uint64_t* fullA = bars;                      // [kGStages] G box landed
+  uint64_t* emptyA = fullA + kGStages;         // [kGStages] MMAs that read it done (commit)
+  uint64_t* fullB = emptyA + kGStages;         // [kTStages] T built (one arrival per builder warp)
+  uint64_t* emptyT = fullB + kTStages;         // [kTStages] MMAs that read it done (commit)
+  uint64_t* fullTab = emptyT + kTStages;       // [kTabSlots] psi block landed
+  uint64_t* emptyTab = fullTab + kTabSlots;    // [kTabSlots] builders done reading (one arrival per warp)
+  uint64_t* info_full = emptyTab + kTabSlots;  // [2] entry list landed
+  uint64_t* info_empty = info_full + 2;        // [2] entry list released by all readers
+  uint64_t* acc_full = info_full + 4;          // all MMAs of a tile done (commit)
+  uint64_t* tmem_empty = info_full + 5;        // epilogue read TMEM out (one arrival per warp)
+  uint64_t* drain = info_full + 6;             // MMAs in flight done, after a failure (commit)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(info_full + 7);
+  int32_t* info_cnt = reinterpret_cast<int32_t*>(info_full + 8);  // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(info_full + 9);
+  volatile int* tile_id = reinterpret_cast<volatile int*>(info_full + 10);  // [2], -1 = no more tiles
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = a.ntx * a.nty * a.ntz;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kGStages; ++s) {
       mbar_init(&fullA[s], 1);
-      mbar_init(&fullT[s], 1);
-      mbar_init(&fullB[s], kBuilderThreads);
-      mbar_init(&empty[s], 1);
+      mbar_init(&emptyA[s], 1);
+    }
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(&fullB[s], kBuilderThreads / 32);
+      mbar_init(&emptyT[s], 1);
+    }
+    for (int s = 0; s < kTabSlots; ++s) {
+      mbar_init(&fullTab[s], 1);
+      mbar_init(&emptyTab[s], kBuilderThreads / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&info_full[b], 1);
-      mbar_init(&info_empty[b], kProducers - 1 + 1 + kBuilderThreads + kEpiThreads);
+      mbar_init(&info_empty[b], kGProducers + 1 + (kBuilderThreads + kEpiThreads) / 32);
     }
     mbar_init(acc_full, 1);
-    mbar_init(tmem_empty, kEpiThreads);
+    mbar_init(tmem_empty, kEpiThreads / 32);
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -218,58 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  // Copies of item i (stage i % kStages): the psi block and the 1-2 G boxes.
-  // Issued by producer i % kProducers after the stage's previous MMAs completed.
-  auto issue_item = [&](int i, const disco_grp_ent& en, int k, int c, int qb, int bc0) -> bool {
-    const int s = i % kStages;
-    if ((i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, kWaitLimit)) || *abort_flag)
-      return false;
-    uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
-    const int nsteps = min(4, (int)en.KB - 4 * c);
-    const int nbox = (4 * c + nsteps + kStep1 + 3) / 4 - c;  // 1 or 2
-    mbar_expect_tx(&fullT[s], Cfg::kTabBytes);
-    const long long toff = (long long)en.off + (long long)(k * en.nch + c) * grp_block(S);
-    if (DISCO_IN_BOUNDS(k >= 0 && k < a.K && c >= 0 && c < en.nch && toff >= 0 && toff + grp_block(S) <= a.ngtab))
-      bulk_copy(st + 2 * kBoxBytes + kTBytes, a.gtab + toff, Cfg::kTabBytes, &fullT[s]);
-    else
-      mbar_complete_tx(&fullT[s], Cfg::kTabBytes);
-    mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
-    const int row = k * a.Hout + en.ho;
-    const bool rows_ok = DISCO_IN_BOUNDS(en.ho >= 0 && en.ho < a.Hout && bc0 >= 0 && bc0 < a.BC);
-    for (int bb = 0; bb < nbox; ++bb) {
-      const int col0 = qb - en.MW + 64 * (c + bb);
-      uint8_t* dst = st + bb * kBoxBytes;
-      if (!box_is_narrow(col0, a.Wout)) {
-        if (DISCO_IN_BOUNDS(rows_ok && wrapc(col0, a.Wout) >= 0))
-          tma_load_3d(dst, &gwide, wrapc(col0, a.Wout), row, bc0, &fullA[s]);
-        else
-          mbar_complete_tx(&fullA[s], kBoxBytes);
-      } else {
-        for (int g = 0; g < 8; ++g) {
-          const int cn = wrapc(col0 + 8 * g, a.Wout);
-          if (DISCO_IN_BOUNDS(rows_ok && cn >= 0 && cn + 8 <= a.Wout))
-            tma_load_3d(dst + g * kNarrowBytes, &gnarrow, cn, row, bc0, &fullA[s]);
-          else
-            mbar_complete_tx(&fullA[s], kNarrowBytes);
-        }
-      }
-    }
-    return true;
-  };
-  // after a failure: let this producer's copies in flight land before the CTA
-  // exits (n = one past its last issued item)
-  auto drain_own = [&](int n, int who) {
-    for (int li = n - 1; li >= 0 && li >= n - kProducers * kStages; --li)
-      if (li % kProducers == who) {
-        mbar_wait(&fullA[li % kStages], (li / kStages) & 1, kWaitLimit);
-        mbar_wait(&fullT[li % kStages], (li / kStages) & 1, kWaitLimit);
-      }
-  };
-
   if (warp == 0) {
-    // ------------------------------------------- producer (items i % 3 == 0) --
+    // ------------------------------------ tiles, entry lists, psi blocks --
     if (lane == 0) {
-      int i = 0, tl = 0, done = 0;  // done: one past the last item this thread issued
+      int i = 0, tl = 0, done = 0;  // done: one past the last item whose psi block was issued
       bool ok = true;
       unsigned long long* slot = sched_join(g_btc_sched, a.launch_id, kWaitLimit);
       if (!slot) btc_flag(kStatusBtcTimeout);  // this CTA takes no tile
@@ -305,17 +302,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_arrive(&info_full[b]);
         }
+        // item (ho, k, c): the psi block of chunk c into psi slot i % kTabSlots
         for (int j = 0; j < ne && ok; ++j) {
           const disco_grp_ent en = info[j];
+          const int nit = entry_items<S>(en);
           for (int k = 0; k < a.K && ok; ++k)
-            for (int c = 0; c < en.nch && ok; ++c, ++i)
-              if (i % kProducers == 0 && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
+            for (int c = 0; c < nit && ok; ++c, ++i) {
+              const int t = i % kTabSlots;
+              if ((i >= kTabSlots && !mbar_wait(&emptyTab[t], ((i / kTabSlots) - 1) & 1, kWaitLimit)) ||
+                  *abort_flag) {
+                ok = false;
+                break;
+              }
+              if (c < en.nch) {
+                mbar_expect_tx(&fullTab[t], Cfg::kTabBytes);
+                const long long toff = (long long)en.off + (long long)(k * en.nch + c) * grp_block(S);
+                if (DISCO_IN_BOUNDS(k >= 0 && k < a.K && c >= 0 && toff >= 0 && toff + grp_block(S) <= a.ngtab))
+                  bulk_copy(smem + Cfg::kTabOff + t * Cfg::kTabBytes, a.gtab + toff, Cfg::kTabBytes, &fullTab[t]);
+                else
+                  mbar_complete_tx(&fullTab[t], Cfg::kTabBytes);
+              } else {
+                mbar_arrive(&fullTab[t]);  // the item past the last chunk builds no T
+              }
+              done = i + 1;
+            }
         }
       }
       if (!ok) {
         btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
-        drain_own(done, 0);
+        // let the copies in flight land before the CTA exits
+        for (int li = done - 1; li >= 0 && li >= done - kTabSlots; --li)
+          mbar_wait(&fullTab[li % kTabSlots], (li / kTabSlots) & 1, kWaitLimit);
       }
       if (slot) sched_leave(slot);
     }
@@ -323,7 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       const uint32_t idesc = idesc_16_f32(128, kN, a.f16 != 0);
-      int i = 0, tl = 0;
+      // Descriptors of the first T chunk and G box (128-byte swizzled).  Stage
+      // x and K step q add x * (stage bytes) / 16 and 2 q (32 bytes a step) to
+      // the start-address field.
+      const uint32_t sb = smem_u32(smem);
+      const uint64_t dT0 = smem_desc_sw128(sb), dG0 = smem_desc_sw128(sb + Cfg::kGOff);
+      // (8 wrapped 8-column boxes: unswizzled, K step q 4 KB further on)
+      const uint64_t dN0 = smem_desc(sb + Cfg::kGOff, kNarrowBytes, 128);
+      constexpr uint64_t kTStep = kTBytes >> 4, kGStep = kBoxBytes >> 4;
+      int i = 0, nb = 0, tl = 0;  // items and G boxes so far
       bool ok = true;
       for (; ok; ++tl) {
         const int b = tl & 1;
@@ -337,44 +363,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        tc_fence_after();
         int qb, bc0, zg;
         tile_coords<S>(a, tile, &qb, &bc0, &zg);
-        tc_fence_after();
         const int ne = info_cnt[b];
         const disco_grp_ent* info = infos + b * kMaxEnt;
-        bool first = true;
+        bool fresh0 = true, fresh1 = true;  // the blocks' accumulators not yet written in this tile
         for (int j = 0; j < ne && ok; ++j) {
-          const disco_grp_ent en = info[j];
-          for (int k = 0; k < a.K && ok; ++k)
-            for (int c = 0; c < en.nch; ++c, ++i) {
-              const int s = i % kStages;
-              const uint32_t ph = (i / kStages) & 1;
-              if (!mbar_wait(&fullA[s], ph, kWaitLimit) || !mbar_wait(&fullB[s], ph, kWaitLimit) ||
-                  *abort_flag) {
+          const int KB = info[j].KB, nit = entry_items<S>(info[j]);
+          const int w0 = wrapc(qb - info[j].MW, a.Wout);  // ring column of box 0
+          for (int k = 0; k < a.K && ok; ++k) {
+            int wc = w0;
+            for (int c = 0; c < nit; ++c, ++i) {
+              // a window chunk across the longitude seam: two boxes, each with
+              // the other's columns zero, and the MMAs run on both (kTwoBox),
+              // or one unswizzled tile of 8 wrapped boxes
+              const bool cross = wc + 64 > a.Wout, seam = kTwoBox && cross;
+              const int g0 = nb % kGStages, g1 = (nb + 1) % kGStages, x = i % kTStages;
+              if (!mbar_wait(&fullA[g0], (nb / kGStages) & 1, kWaitLimit) ||
+                  (seam && !mbar_wait(&fullA[g1], ((nb + 1) / kGStages) & 1, kWaitLimit)) ||
+                  !mbar_wait(&fullB[x], (i / kTStages) & 1, kWaitLimit) || *abort_flag) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t sbase = smem_u32(smem + (size_t)s * Cfg::kStageBytes);
-              const uint32_t tbase = sbase + 2 * kBoxBytes;
-              const bool narrow0 = box_is_narrow(qb - en.MW + 64 * c, a.Wout);
-              const bool narrow1 = box_is_narrow(qb - en.MW + 64 * (c + 1), a.Wout);
-              const int nsteps = min(4, (int)en.KB - 4 * c);
-              for (int t = 0; t < nsteps; ++t) {
-                const uint64_t bd = smem_desc_sw128(tbase + 32 * t);
-                for (int blk = 0; blk < kNT; ++blk) {
-                  const int as = t + blk * kStep1;  // K step within the chunk's boxes
-                  const int bb = as >> 2, ka = as & 3;
-                  const uint32_t slot = sbase + bb * kBoxBytes;
-                  const uint64_t ad = (bb ? narrow1 : narrow0)
-                                          ? smem_desc(slot + ka * 2 * kNarrowBytes, kNarrowBytes, 128)
-                                          : smem_desc_sw128(slot + 32 * ka);
-                  umma_bf16(tmem + blk * kN, ad, bd, idesc, (first && t == 0) ? 0u : 1u);
+              const uint64_t dT = dT0 + x * kTStep;
+              // T chunk c - 1 (item i - 1, read when c >= 1): its last kStep1 steps
+              const uint64_t dTp = dT0 + ((i + kTStages - 1) % kTStages) * kTStep;
+              const uint64_t dA0 = (!kTwoBox && cross ? dN0 : dG0) + g0 * kGStep, dA1 = dG0 + g1 * kGStep;
+              const uint32_t dAq = !kTwoBox && cross ? 256u : 2u;
+              // box step q holds window step w = 4 c + q: block 0 pairs it with
+              // T step w (this chunk's step q), block 1 with T step w - kStep1
+              // (this chunk's step q - kStep1, or chunk c - 1's step 4 + q - kStep1)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int w = 4 * c + q, t1 = w - kStep1;
+                if (w < KB) {
+                  umma_bf16(tmem, dA0 + q * dAq, dT + 2 * q, idesc, fresh0 ? 0u : 1u);
+                  if (seam) umma_bf16(tmem, dA1 + 2 * q, dT + 2 * q, idesc, 1u);
+                  fresh0 = false;
+                }
+                if (t1 >= 0 && t1 < KB) {
+                  const uint64_t bd = q >= kStep1 ? dT + 2 * (q - kStep1) : dTp + 2 * (4 + q - kStep1);
+                  umma_bf16(tmem + kN, dA0 + q * dAq, bd, idesc, fresh1 ? 0u : 1u);
+                  if (seam) umma_bf16(tmem + kN, dA1 + 2 * q, bd, idesc, 1u);
+                  fresh1 = false;
                 }
               }
-              first = false;
-              umma_commit(&empty[s]);
+              // item i's G boxes, and item i - 1's T chunk (whose last steps
+              // item i read), are free once these MMAs complete
+              umma_commit(&emptyA[g0]);
+              if (seam) umma_commit(&emptyA[g1]);
+              if (i >= 1) umma_commit(&emptyT[(i + kTStages - 1) % kTStages]);
+              nb += seam ? 2 : 1;
+              wc = wc + 64 >= a.Wout ? wc + 64 - a.Wout : wc + 64;
             }
+          }
         }
         if (!ok) break;
         mbar_arrive(&info_empty[b]);
@@ -384,13 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
-        if (i > 0)  // let the MMAs in flight finish before TMEM is freed
-          mbar_wait(&empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, kWaitLimit);
+        // let the MMAs in flight finish before TMEM is freed
+        umma_commit(drain);
+        mbar_wait(drain, 0, kWaitLimit);
       }
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------- T builders (6 warps) --
-    const int btid = tid - 64;
+  } else if ((warp != 5 && warp < 8) || warp == 12) {
+    // -------------------------------- T builders (warps 2, 3, 4, 6, 7, 12) --
+    const int btid = 32 * (warp == 12 ? 5 : warp < 5 ? warp - 2 : warp - 3) + lane;
     int i = 0, tl = 0;
     bool ok = true;
     for (; ok; ++tl) {
@@ -404,19 +449,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ne = info_cnt[b];
       const disco_grp_ent* info = infos + b * kMaxEnt;
       for (int j = 0; j < ne && ok; ++j) {
-        const int KB = info[j].KB, nch = info[j].nch;
+        const int KB = info[j].KB, nch = info[j].nch, nit = entry_items<S>(info[j]);
         for (int k = 0; k < a.K && ok; ++k)
-          for (int c = 0; c < nch; ++c, ++i) {
-            const int s = i % kStages;
-            // the stage's copies are issued only after the MMAs of its previous item
-            // completed; T needs only the psi block
-            const bool mine = mbar_wait(&fullT[s], (i / kStages) & 1, kWaitLimit) && !*abort_flag;
+          for (int c = 0; c < nit; ++c, ++i) {
+            const int t = i % kTabSlots, x = i % kTStages;
+            // the item's psi block has landed and the MMAs that read the T
+            // stage's previous chunk are done
+            const bool mine = mbar_wait(&fullTab[t], (i / kTabSlots) & 1, kWaitLimit) &&
+                              (i < kTStages || mbar_wait(&emptyT[x], ((i / kTStages) - 1) & 1, kWaitLimit)) &&
+                              !*abort_flag;
             ok = all_named(mine, 1, kBuilderThreads);
             if (!ok) break;
-            uint8_t* st = smem + (size_t)s * Cfg::kStageBytes;
-            uint8_t* T = st + 2 * kBoxBytes;
-            const uint16_t* tab = reinterpret_cast<const uint16_t*>(st + 2 * kBoxBytes + kTBytes);
-            const int nq = 2 * min(4, KB - 4 * c);  // 16-byte chunks per T row
+            uint8_t* T = smem + x * kTBytes;
+            const uint16_t* tab = reinterpret_cast<const uint16_t*>(smem + Cfg::kTabOff + t * Cfg::kTabBytes);
+            // 16-byte chunks per T row (none for the item past the last chunk)
+            const int nq = c < nch ? 2 * min(4, KB - 4 * c) : 0;
             // T[(r, t, p), 8 q8 + e] = tab[r][p][8 q8 + TQ - 1 - t + e]: the rows
             // t = 8 g + j (j = 0..7) of one (r, p, q8) read the same 16 table
             // values from the aligned index 8 q8 + TQ - 8 - 8 g on, shifted by
@@ -442,22 +489,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(T + n * 128 + ((q8 ^ (n & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
               }
             }
+            // every thread's T writes are visible to the tensor cores, then one
+            // arrival per warp (192 arrivals on one barrier would serialise)
             fence_proxy_async_smem();
-            mbar_arrive(&fullB[s]);
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&fullB[x]);
+              mbar_arrive(&emptyTab[t]);
+            }
           }
       }
       if (!ok) break;
-      mbar_arrive(&info_empty[b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&info_empty[b]);
     }
     if (!ok) {
       btc_flag(kStatusBtcTimeout);
       *abort_flag = 1;
     }
-  } else if (warp >= 12) {
-    // ----------------------------------- producers of items i % 3 == 1, 2 --
-    const int who = warp - 11;
+  } else if (warp == 5 || warp == 13) {
+    // ------------------------------ G producers (warps 5, 13): boxes n % 2 --
+    // One 64-column box per item (with kTwoBox two where the window chunk
+    // crosses the longitude seam: the box at the chunk's ring column, whose
+    // columns past the seam are outside the tensor and arrive as zeros, and
+    // the box one ring earlier, whose columns before the seam arrive as
+    // zeros) into G stage n % kGStages, n counting boxes, as soon as the MMAs
+    // that read the stage's previous box are done.
+    const int who = warp == 5 ? 0 : 1;
     if (lane == 0) {
-      int i = 0, done = 0;
+      int i = 0, nb = 0, done = 0;  // done: one past the last box this thread issued
       bool ok = true;
       for (int tl = 0; ok; ++tl) {
         const int b = tl & 1;
@@ -473,9 +533,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const disco_grp_ent* info = infos + b * kMaxEnt;
         for (int j = 0; j < ne && ok; ++j) {
           const disco_grp_ent en = info[j];
-          for (int k = 0; k < a.K && ok; ++k)
-            for (int c = 0; c < en.nch && ok; ++c, ++i)
-              if (i % kProducers == who && (ok = issue_item(i, en, k, c, qb, bc0))) done = i + 1;
+          const int nit = entry_items<S>(en);
+          const int w0 = wrapc(qb - en.MW, a.Wout);
+          [[maybe_unused]] const bool rows_ok =
+              DISCO_IN_BOUNDS(en.ho >= 0 && en.ho < a.Hout && bc0 >= 0 && bc0 < a.BC);
+          for (int k = 0; k < a.K && ok; ++k) {
+            const int grow = k * a.Hout + en.ho;
+            int wc = w0;
+            for (int c = 0; c < nit && ok; ++c, ++i) {
+              const bool cross = wc + 64 > a.Wout;
+              const int nbox = kTwoBox && cross ? 2 : 1;
+              for (int h = 0; h < nbox; ++h, ++nb) {
+                if (nb % kGProducers != who) continue;
+                const int g = nb % kGStages;
+                if ((nb >= kGStages && !mbar_wait(&emptyA[g], ((nb / kGStages) - 1) & 1, kWaitLimit)) ||
+                    *abort_flag) {
+                  ok = false;
+                  break;
+                }
+                uint8_t* dst = smem + Cfg::kGOff + g * kBoxBytes;
+                mbar_expect_tx(&fullA[g], kBoxBytes);
+                if (kTwoBox || !cross) {
+                  const int x0 = h == 0 ? wc : wc - a.Wout;  // the second box starts before column 0
+                  if (DISCO_IN_BOUNDS(rows_ok && x0 > -64 && x0 < a.Wout))
+                    tma_load_3d(dst, &gwide, x0, grow, bc0, &fullA[g]);
+                  else
+                    mbar_complete_tx(&fullA[g], kBoxBytes);
+                } else {
+                  for (int q = 0; q < 8; ++q) {
+                    const int cn = wrapc(wc + 8 * q, a.Wout);
+                    if (DISCO_IN_BOUNDS(rows_ok && cn >= 0 && cn + 8 <= a.Wout))
+                      tma_load_3d(dst + q * kNarrowBytes, &gnarrow, cn, grow, bc0, &fullA[g]);
+                    else
+                      mbar_complete_tx(&fullA[g], kNarrowBytes);
+                  }
+                }
+                done = nb + 1;
+              }
+              wc = wc + 64 >= a.Wout ? wc + 64 - a.Wout : wc + 64;
+            }
+          }
         }
         if (!ok) break;
         mbar_arrive(&info_empty[b]);
@@ -483,7 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         btc_flag(kStatusBtcTimeout);
         *abort_flag = 1;
-        drain_own(done, who);
+        // let this thread's boxes in flight land before the CTA exits
+        for (int lb = done - 1; lb >= 0 && lb >= done - kGStages; --lb)
+          if (lb % kGProducers == who) mbar_wait(&fullA[lb % kGStages], (lb / kGStages) & 1, kWaitLimit);
       }
     }
   } else {
@@ -554,8 +653,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       tc_fence_before();
-      mbar_arrive(tmem_empty);
-      mbar_arrive(&info_empty[b]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(tmem_empty);
+        mbar_arrive(&info_empty[b]);
+      }
     }
     if (tid == 256) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
@@ -654,7 +756,7 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
                                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
   }
-  auto kern = bwd_tc_kernel<S>;
+  auto kern = roc ? bwd_tc_kernel<S, false> : bwd_tc_kernel<S, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) != cudaSuccess)
     return check_launch("disco_bwd (tensor cores) attribute");
   const long long ntiles = (long long)a.ntx * a.nty * a.ntz;

@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
           for (int bb = 0; bb < nbox; ++bb) {
             const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
-            const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
+            [[maybe_unused]] const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
             if (col + 64 <= a.Win) {
               if (DISCO_IN_BOUNDS(rows_ok && col >= 0))
                 tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
@@ -588,8 +588,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
   auto coords = [&](int t, int* ho, int* bc0, int* wc) {
     *wc = (t % ntx) * (kTW * NT);
     const int r = t / ntx;
-    *bc0 = (r % nty) * 128;
-    *ho = a.row_order[r / nty];
+    *bc0 = (r / a.Hout) * 128;
+    *ho = a.row_order[r % a.Hout];
     if (!DISCO_IN_BOUNDS(*ho >= 0 && *ho < a.Hout)) *ho = 0;
   };
   // runs of output row ho; every role clips a bad range the same way
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_expect_tx(&fullA[s], nbox * kBoxBytes);
             for (int bb = 0; bb < nbox; ++bb) {
               const int col = wrap_col(u0 + c * kChunkCols + 64 * bb, a.Win);
-              const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
+              [[maybe_unused]] const bool rows_ok = DISCO_IN_BOUNDS(g.hi >= 0 && g.hi < a.Hin && bc0 >= 0 && bc0 < a.BC);
               if (col + 64 <= a.Win) {
                 if (DISCO_IN_BOUNDS(rows_ok && col >= 0))
                   tma_load_3d(sA + bb * kBoxBytes, &xmap, col, g.hi, bc0, &fullA[s]);
