@@ -110,7 +110,8 @@ typedef struct {
   int16_t MW;   /* window half-width in output columns, a multiple of 8 */
   int16_t KB;   /* 16-column steps of one tile block: ceil((TQ + 2 MW) / 16) */
   int16_t nch;  /* 64-column chunks: ceil(KB / 4) */
-  int16_t pad;
+  int8_t r0;    /* first and last input row of the group (0 .. 7) with psi */
+  int8_t r1;    /*   support at this output row: the rows the entry's tiles cover */
 } disco_grp_ent;
 
 /* psi: sizes set by disco_psi_plan, device pointers (into the caller's psi

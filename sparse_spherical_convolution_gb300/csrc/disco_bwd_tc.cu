@@ -88,12 +88,7 @@ constexpr int kBuilderThreads = 192;        // warps 2, 3, 4, 6, 7, 12
 constexpr int kEpiThreads = 128;            // warps 8-11
 constexpr int kN = 256;                     // MMA N = 8 rows x 32 columns
 constexpr int kNT = 2;                      // column blocks per tile
-constexpr int kTStages = 4;                 // T chunks: built ahead, and kept for the next item
-constexpr int kGStages = 4;                 // G boxes: in flight from L2 or waiting for their MMAs
 constexpr int kTabSlots = 4;                // psi blocks fetched ahead of the builders
-// a G producer waits on the G stage of its own earlier item: every G stage must
-// stay with one producer, or it would wait on a phase of another producer's item
-static_assert(kGStages % kGProducers == 0, "a G stage stays with one G producer");
 constexpr int kMaxEnt = 128;                // entries (output rows) of one group
 constexpr uint32_t kBoxBytes = 128 * 128;   // 128 channels x 64 columns bf16
 constexpr uint32_t kNarrowBytes = 128 * 16; // 128 channels x 8 columns
@@ -153,11 +148,32 @@ struct BtcArgs {
 };
 
 template <int S>
-struct BCfg {
+struct BGeom {
   static constexpr int TQ = grp_tq(S);
   static constexpr int CW = grp_cw(S);
   static constexpr int kStep1 = TQ / 16;  // K steps between the two blocks' windows (1 or 2)
   static constexpr uint32_t kTabBytes = (uint32_t)grp_block(S) * 2;  // the psi block of one chunk
+};
+
+#ifndef KTP
+#define KTP 3
+#endif
+#ifndef KGP
+#define KGP 6
+#endif
+template <int S, bool kTwoBox>
+struct BCfg : BGeom<S> {
+  using BGeom<S>::kTabBytes;
+  // Ring depths.  T chunks: built ahead of the MMAs and kept for the next
+  // item.  G boxes: in flight from L2 or waiting for their MMAs; with two
+  // boxes for each window chunk across the seam (kTwoBox) the G ring is
+  // deeper, or the items of the tiles at the seam would wait on the round
+  // trip from an item's MMAs to the next boxes.
+  static constexpr int kTStages = kTwoBox ? KTP : 4;
+  static constexpr int kGStages = kTwoBox ? KGP : 4;
+  // a G producer waits on the G stage of its own earlier box: every G stage
+  // must stay with one producer, or it would wait on a phase of another's box
+  static_assert(kGStages % kGProducers == 0, "a G stage stays with one G producer");
   // layout: T stages | G stages | psi slots | entry lists | gx pieces | barriers
   static constexpr uint32_t kGOff = kTStages * kTBytes;
   static constexpr uint32_t kTabOff = kGOff + kGStages * kBoxBytes;
@@ -169,6 +185,7 @@ struct BCfg {
   static constexpr size_t kSmem = (size_t)kBarOff + 512 + 1024;  // + barriers, + alignment slack
   static_assert(kGOff % 1024 == 0 && kTabBytes % 16 == 0 && kInfoOff % 16 == 0 && kOutOff % 128 == 0,
                 "alignment of the swizzled tiles and copy targets");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // the z-th row group in processing order: poles first, then inwards, so the
@@ -181,7 +198,7 @@ __device__ __forceinline__ void tile_coords(const BtcArgs& a, int tile, int* qb,
   const int rest = tile / a.ntx;
   const int z = rest % a.ntz;
   const int y = rest / a.ntz;
-  *qb = x * (kNT * BCfg<S>::TQ);
+  *qb = x * (kNT * BGeom<S>::TQ);
   *bc0 = y * 128;
   *zg = row_group(z, a.ntz);
 }
@@ -191,7 +208,7 @@ __device__ __forceinline__ void tile_coords(const BtcArgs& a, int tile, int* qb,
 // KB-1+kStep1, so the window spans KB + kStep1 steps of 16 columns.
 template <int S>
 __device__ __forceinline__ int entry_items(const disco_grp_ent& en) {
-  return ((int)en.KB + BCfg<S>::kStep1 + 3) / 4;
+  return ((int)en.KB + BGeom<S>::kStep1 + 3) / 4;
 }
 
 // kTwoBox: a window chunk across the longitude seam arrives as two zero-padded
@@ -203,8 +220,9 @@ template <int S, bool kTwoBox>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap gwide, const __grid_constant__ CUtensorMap gnarrow,
                   const __grid_constant__ CUtensorMap gxmap, const BtcArgs a) {
-  using Cfg = BCfg<S>;
+  using Cfg = BCfg<S, kTwoBox>;
   constexpr int TQ = Cfg::TQ, CW = Cfg::CW;
+  constexpr int kTStages = Cfg::kTStages, kGStages = Cfg::kGStages;
   constexpr int kStep1 = Cfg::kStep1;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
@@ -340,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      const uint32_t idesc = idesc_16_f32(128, kN, a.f16 != 0);
       // Descriptors of the first T chunk and G box (128-byte swizzled).  Stage
       // x and K step q add x * (stage bytes) / 16 and 2 q (32 bytes a step) to
       // the start-address field.
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int tile = tile_id[b];
         if (tile < 0) break;
-        if ((tl >= 1 && !mbar_wait(tmem_empty, (tl - 1) & 1, kWaitLimit)) || *abort_flag) {
+        if (!mbar_wait(tmem_empty, tl & 1, kWaitLimit) || *abort_flag) {  // TMEM read out and zeroed
           ok = false;
           break;
         }
@@ -368,10 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords<S>(a, tile, &qb, &bc0, &zg);
         const int ne = info_cnt[b];
         const disco_grp_ent* info = infos + b * kMaxEnt;
-        bool fresh0 = true, fresh1 = true;  // the blocks' accumulators not yet written in this tile
         for (int j = 0; j < ne && ok; ++j) {
           const int KB = info[j].KB, nit = entry_items<S>(info[j]);
           const int w0 = wrapc(qb - info[j].MW, a.Wout);  // ring column of box 0
+          // only the rows r0 .. r1 of the group have support at this output
+          // row: MMAs of N = 32 (r1 - r0 + 1) on T rows and TMEM columns from 32 r0
+          const int r0 = info[j].r0, nr = info[j].r1 - r0 + 1;
+          const uint32_t ide = idesc_16_f32(128, 32 * nr, a.f16 != 0);
+          const uint32_t d0 = tmem + 32 * r0, d1 = tmem + kN + 32 * r0;
+          const uint64_t toff = 256u * r0;  // 4 KB of T rows per input row
           for (int k = 0; k < a.K && ok; ++k) {
             int wc = w0;
             for (int c = 0; c < nit; ++c, ++i) {
@@ -387,27 +409,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint64_t dT = dT0 + x * kTStep;
+              const uint64_t dT = dT0 + x * kTStep + toff;
               // T chunk c - 1 (item i - 1, read when c >= 1): its last kStep1 steps
-              const uint64_t dTp = dT0 + ((i + kTStages - 1) % kTStages) * kTStep;
+              const uint64_t dTp = dT0 + ((i + kTStages - 1) % kTStages) * kTStep + toff;
               const uint64_t dA0 = (!kTwoBox && cross ? dN0 : dG0) + g0 * kGStep, dA1 = dG0 + g1 * kGStep;
               const uint32_t dAq = !kTwoBox && cross ? 256u : 2u;
               // box step q holds window step w = 4 c + q: block 0 pairs it with
               // T step w (this chunk's step q), block 1 with T step w - kStep1
               // (this chunk's step q - kStep1, or chunk c - 1's step 4 + q - kStep1)
+              // A seam item's second box in a second pass, so that consecutive
+              // MMAs keep alternating between the two accumulators (MMAs into
+              // one accumulator back to back ran at well under half the rate;
+              // skipping the K steps that lie wholly in a box's zero columns
+              // made the pass slower, not faster).
+              for (int pass = 0; pass < (seam ? 2 : 1); ++pass) {
+                const uint64_t dA = pass ? dA1 : dA0;
+                const uint32_t dq = pass ? 2u : dAq;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int w = 4 * c + q, t1 = w - kStep1;
-                if (w < KB) {
-                  umma_bf16(tmem, dA0 + q * dAq, dT + 2 * q, idesc, fresh0 ? 0u : 1u);
-                  if (seam) umma_bf16(tmem, dA1 + 2 * q, dT + 2 * q, idesc, 1u);
-                  fresh0 = false;
-                }
-                if (t1 >= 0 && t1 < KB) {
-                  const uint64_t bd = q >= kStep1 ? dT + 2 * (q - kStep1) : dTp + 2 * (4 + q - kStep1);
-                  umma_bf16(tmem + kN, dA0 + q * dAq, bd, idesc, fresh1 ? 0u : 1u);
-                  if (seam) umma_bf16(tmem + kN, dA1 + 2 * q, bd, idesc, 1u);
-                  fresh1 = false;
+                for (int q = 0; q < 4; ++q) {
+                  const int w = 4 * c + q, t1 = w - kStep1;
+                  if (w < KB) umma_bf16(d0, dA + q * dq, dT + 2 * q, ide, 1u);
+                  if (t1 >= 0 && t1 < KB)
+                    umma_bf16(d1, dA + q * dq, q >= kStep1 ? dT + 2 * (q - kStep1) : dTp + 2 * (4 + q - kStep1),
+                              ide, 1u);
                 }
               }
               // item i's G boxes, and item i - 1's T chunk (whose last steps
@@ -450,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const disco_grp_ent* info = infos + b * kMaxEnt;
       for (int j = 0; j < ne && ok; ++j) {
         const int KB = info[j].KB, nch = info[j].nch, nit = entry_items<S>(info[j]);
+        const int r0 = info[j].r0, nr = info[j].r1 - r0 + 1;  // the rows the MMAs read
         for (int k = 0; k < a.K && ok; ++k)
           for (int c = 0; c < nit; ++c, ++i) {
             const int t = i % kTabSlots, x = i % kTStages;
@@ -469,11 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // values from the aligned index 8 q8 + TQ - 8 - 8 g on, shifted by
             // 7 - j.  One unit (r, p, g, q8) loads them with two 16-byte loads
             // and writes the 8 rows' chunks q8; q8 varies fastest across lanes
-            // (conflict-free loads, and stores that cover all banks)
+            // (conflict-free loads, and stores that cover all banks).  Only the
+            // rows r0 .. r1 are built: the MMAs read no others
             constexpr int kG = TQ / 8;  // row groups of 8 t per (r, p)
-            for (int u = btid; u < 8 * S * kG * nq; u += kBuilderThreads) {
+            for (int u = btid; u < nr * S * kG * nq; u += kBuilderThreads) {
               const int q8 = u % nq, rest = u / nq;
-              const int g = rest % kG, rp = rest / kG;  // rp = r S + p
+              const int g = rest % kG, rp = rest / kG + r0 * S;  // rp = r S + p
               const int r = rp / S, p = rp - r * S;
               const uint4* src = reinterpret_cast<const uint4*>(tab + rp * CW + 8 * (q8 + kG - 1 - g));
               const uint4 lo = src[0], hi = src[1];
@@ -588,6 +614,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ----------------------------------------------- epilogue (warps 8-11) --
     const int q = warp & 3;
+    // The MMAs accumulate into TMEM that the epilogue leaves zero: cleared here
+    // for the first tile, and after reading each tile out for the next one
+    // (a tile's entries cover different rows, so no MMA may start a sum).
+    for (int col = 0; col < 2 * kN; col += 16) tmem_st16_zero(tmem + ((uint32_t)(q * 32) << 16) + col);
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tmem_empty);
     int tl = 0, npiece = 0;
     for (;; ++tl) {
       const int b = tl & 1;
@@ -624,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cc = 0; cc < 2; ++cc) {
             float v[16];
             if (any) {
-              tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + blk * kN + r * 32 + cc * 16, v);
+              const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + blk * kN + r * 32 + cc * 16;
+              tmem_ld16(ta, v);
+              tmem_st16_zero(ta);
             } else {
 #pragma unroll
               for (int e = 0; e < 16; ++e) v[e] = 0.f;
@@ -652,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -721,7 +758,6 @@ int encode_g(CUtensorMap* map, const void* G, const BtcArgs& a, int BC, int boxw
 
 template <int S>
 int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool roc, bool f16) {
-  using Cfg = BCfg<S>;
   BtcArgs a;
   a.gx = (__nv_bfloat16*)gx;
   a.grp_ptr = psi->grp_ptr;
@@ -734,7 +770,7 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
   a.Hout = psi->grid_out.nlat;
   a.Wout = psi->grid_out.nlon;
   a.K = psi->K;
-  a.ntx = (a.Win + S * kNT * Cfg::TQ - 1) / (S * kNT * Cfg::TQ);
+  a.ntx = (a.Win + S * kNT * BGeom<S>::TQ - 1) / (S * kNT * BGeom<S>::TQ);
   a.nty = (BC + 127) / 128;
   a.ntz = psi->ngrp;
   a.ngrp_ent = psi->ngrp_ent;
@@ -757,13 +793,14 @@ int launch_btc(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream
     if (cr != CUDA_SUCCESS) return fail(DISCO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)cr);
   }
   auto kern = roc ? bwd_tc_kernel<S, false> : bwd_tc_kernel<S, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem) != cudaSuccess)
+  const size_t smem = roc ? BCfg<S, false>::kSmem : BCfg<S, true>::kSmem;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return check_launch("disco_bwd (tensor cores) attribute");
   const long long ntiles = (long long)a.ntx * a.nty * a.ntz;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
   if (ntiles + grid > (long long)kSchedCountMask || grid > kSchedMaxCtas)
     return fail(DISCO_ERR_UNSUPPORTED, "problem too large");
-  kern<<<grid, kThreads, Cfg::kSmem, st>>>(wide, narrow, gxm, a);
+  kern<<<grid, kThreads, smem, st>>>(wide, narrow, gxm, a);
   return check_launch("disco_bwd (tensor cores)");
 }
 
@@ -799,7 +836,6 @@ bool bwd_tc_supported(const disco_psi* psi, int BC) {
 int bwd_tensor_core(const disco_psi* psi, const void* G, void* gx, int BC, cudaStream_t st, bool rows_of_channels,
                     bool f16) {
   if (!bwd_tc_supported(psi, BC) || (f16 && !psi->gtab_h)) return DISCO_ERR_UNSUPPORTED;
-  static_assert(BCfg<1>::kSmem <= 227 * 1024 && BCfg<2>::kSmem <= 227 * 1024, "shared memory");
   return psi->s == 1 ? launch_btc<1>(psi, G, gx, BC, st, rows_of_channels, f16)
                      : launch_btc<2>(psi, G, gx, BC, st, rows_of_channels, f16);
 }

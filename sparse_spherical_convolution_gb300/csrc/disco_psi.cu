@@ -496,21 +496,27 @@ __global__ void table_tail_kernel(PsiGeom g, Workspace ws, PsiOut p, int32_t nru
 
 // ---- transpose tables by input-row group (see disco_psi.grp_ptr) --------
 
-// Walks the output rows that input-row group z reads, calling f(ho, MW, KB, nch).
+// Walks the output rows that input-row group z reads, calling
+// f(ho, MW, KB, nch, r0, r1) with r0 .. r1 the group's rows (0 .. 7) that have
+// support at ho.
 template <typename F>
 __device__ void for_group_rows(const PsiGeom& g, const Workspace& ws, int z, F f) {
   const int s = g.Win / g.Wout, TQ = grp_tq(s);
   const int h0 = z * kGrpRows, h1 = min(g.Hin, h0 + kGrpRows);
   for (int ho = 0; ho < g.Hout; ++ho) {
-    int E = -1;
+    int E = -1, r0 = kGrpRows, r1 = -1;
     for (int hi = h0; hi < h1; ++hi) {
       const int m = ws.mtab[(size_t)ho * g.Hin + hi];
-      if (m >= 0) E = max(E, run_halfwidth(m, g.Win, s));
+      if (m >= 0) {
+        E = max(E, run_halfwidth(m, g.Win, s));
+        r0 = min(r0, hi - h0);
+        r1 = hi - h0;
+      }
     }
     if (E < 0) continue;
     const int MW = (E + 7) & ~7;
     const int KB = (TQ + 2 * MW + 15) / 16;
-    f(ho, MW, KB, (KB + 3) / 4);
+    f(ho, MW, KB, (KB + 3) / 4, r0, r1);
   }
 }
 
@@ -519,7 +525,7 @@ __global__ void gcount_kernel(PsiGeom g, Workspace ws) {
   const int z = blockIdx.x * blockDim.x + threadIdx.x;
   if (z >= num_groups(g)) return;
   int ent = 0, blk = 0;
-  for_group_rows(g, ws, z, [&](int, int, int, int nch) {
+  for_group_rows(g, ws, z, [&](int, int, int, int nch, int, int) {
     ++ent;
     blk += g.K * nch;
   });
@@ -545,14 +551,15 @@ __global__ void gent_kernel(PsiGeom g, Workspace ws, PsiOut p) {
   if (z >= num_groups(g)) return;
   const int blk = grp_block(g.Win / g.Wout);
   int e = p.grp_ptr[z], b = ws.gboff[z];
-  for_group_rows(g, ws, z, [&](int ho, int MW, int KB, int nch) {
+  for_group_rows(g, ws, z, [&](int ho, int MW, int KB, int nch, int r0, int r1) {
     disco_grp_ent en;
     en.ho = ho;
     en.off = b * blk;
     en.MW = (int16_t)MW;
     en.KB = (int16_t)KB;
     en.nch = (int16_t)nch;
-    en.pad = 0;
+    en.r0 = (int8_t)r0;
+    en.r1 = (int8_t)r1;
     if (DISCO_IN_BOUNDS(e >= 0 && e < p.ngrp_ent)) p.grp[e] = en;
     ++e;
     b += g.K * nch;

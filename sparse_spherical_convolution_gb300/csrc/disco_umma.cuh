@@ -162,6 +162,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// Zeros into 16 consecutive columns of the warp's 32 lanes (32 lanes x 32
+// bits); complete them with tmem_st_wait before another thread relies on them.
+__device__ __forceinline__ void tmem_st16_zero(uint32_t taddr) {
+  const uint32_t z = 0u;
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
+      "%1, %1};" ::"r"(taddr),
+      "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // 32 lanes x 32 bits, 16 consecutive columns per thread.  The load and its
 // wait are one asm statement, so no use of the registers can be scheduled
 // before the wait.

@@ -179,6 +179,9 @@ def _check_group_tables(psi, ext, gi, go):
                     if h2 == ho and hi in rows)
             assert MW == (E + 7) // 8 * 8
             assert KB == (TQ + 2 * MW + 15) // 16 and nch == (KB + 3) // 4
+            # the first and last row of the group with support at ho
+            sup = [r for r, hi in enumerate(rows) if (ho, hi) in ext]
+            assert ((int(e[3]) >> 16) & 0xFF, (int(e[3]) >> 24) & 0xFF) == (sup[0], sup[-1])
             assert off == off_next
             off_next += K * nch * BLK
             want_b = np.zeros((K, nch, 8, s, CW), np.int16)
