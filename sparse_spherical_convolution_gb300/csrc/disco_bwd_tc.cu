@@ -414,24 +414,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t dTp = dT0 + ((i + kTStages - 1) % kTStages) * kTStep + toff;
               const uint64_t dA0 = (!kTwoBox && cross ? dN0 : dG0) + g0 * kGStep, dA1 = dG0 + g1 * kGStep;
               const uint32_t dAq = !kTwoBox && cross ? 256u : 2u;
-              // box step q holds window step w = 4 c + q: block 0 pairs it with
-              // T step w (this chunk's step q), block 1 with T step w - kStep1
-              // (this chunk's step q - kStep1, or chunk c - 1's step 4 + q - kStep1)
-              // A seam item's second box in a second pass, so that consecutive
-              // MMAs keep alternating between the two accumulators (MMAs into
-              // one accumulator back to back ran at well under half the rate;
-              // skipping the K steps that lie wholly in a box's zero columns
-              // made the pass slower, not faster).
+              // Box step q holds window step 4 c + q.  T step t = 4 c + m meets
+              // it in block 0 at box step m and in block 1 at box step
+              // m + kStep1 (T step t is this chunk's step m, or for m < 0 chunk
+              // c - 1's step 4 + m).  Issued by T step, the MMAs alternate
+              // between the two accumulators: MMAs into one accumulator back to
+              // back run at well under half the rate.  A seam item's second box
+              // in a second pass, in the same order (skipping the K steps that
+              // lie wholly in a box's zero columns made the pass slower).
               for (int pass = 0; pass < (seam ? 2 : 1); ++pass) {
                 const uint64_t dA = pass ? dA1 : dA0;
                 const uint32_t dq = pass ? 2u : dAq;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const int w = 4 * c + q, t1 = w - kStep1;
-                  if (w < KB) umma_bf16(d0, dA + q * dq, dT + 2 * q, ide, 1u);
-                  if (t1 >= 0 && t1 < KB)
-                    umma_bf16(d1, dA + q * dq, q >= kStep1 ? dT + 2 * (q - kStep1) : dTp + 2 * (4 + q - kStep1),
-                              ide, 1u);
+                for (int m = -kStep1; m < 4; ++m) {
+                  const int t = 4 * c + m;
+                  if (t < 0 || t >= KB) continue;
+                  const uint64_t bd = m >= 0 ? dT + 2 * m : dTp + 2 * (4 + m);
+                  if (m >= 0) umma_bf16(d0, dA + m * dq, bd, ide, 1u);
+                  if (m + kStep1 < 4) umma_bf16(d1, dA + (m + kStep1) * dq, bd, ide, 1u);
                 }
               }
               // item i's G boxes, and item i - 1's T chunk (whose last steps
