@@ -383,6 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         int qb, bc0, zg;
         tile_coords<S>(a, tile, &qb, &bc0, &zg);
+        // block 1 of the last column tile can lie past the ring (W_in / 32 odd):
+        // its MMAs are skipped (the epilogue stores no such piece)
+        const bool blk1 = S * (qb + TQ) < a.Win;
         const int ne = info_cnt[b];
         const disco_grp_ent* info = infos + b * kMaxEnt;
         for (int j = 0; j < ne && ok; ++j) {
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (t < 0 || t >= KB) continue;
                   const uint64_t bd = m >= 0 ? dT + 2 * m : dTp + 2 * (4 + m);
                   if (m >= 0) umma_bf16(d0, dA + m * dq, bd, ide, 1u);
-                  if (m + kStep1 < 4) umma_bf16(d1, dA + (m + kStep1) * dq, bd, ide, 1u);
+                  if (m + kStep1 < 4 && blk1) umma_bf16(d1, dA + (m + kStep1) * dq, bd, ide, 1u);
                 }
               }
               // item i's G boxes, and item i - 1's T chunk (whose last steps
