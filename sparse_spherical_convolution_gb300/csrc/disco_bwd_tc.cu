@@ -155,22 +155,16 @@ struct BGeom {
   static constexpr uint32_t kTabBytes = (uint32_t)grp_block(S) * 2;  // the psi block of one chunk
 };
 
-#ifndef KTP
-#define KTP 3
-#endif
-#ifndef KGP
-#define KGP 6
-#endif
 template <int S, bool kTwoBox>
 struct BCfg : BGeom<S> {
   using BGeom<S>::kTabBytes;
-  // Ring depths.  T chunks: built ahead of the MMAs and kept for the next
-  // item.  G boxes: in flight from L2 or waiting for their MMAs; with two
-  // boxes for each window chunk across the seam (kTwoBox) the G ring is
-  // deeper, or the items of the tiles at the seam would wait on the round
-  // trip from an item's MMAs to the next boxes.
-  static constexpr int kTStages = kTwoBox ? KTP : 4;
-  static constexpr int kGStages = kTwoBox ? KGP : 4;
+  // Ring depths (as much as shared memory holds).  T chunks: built ahead of
+  // the MMAs and kept for the next item.  G boxes: in flight from L2 or
+  // waiting for their MMAs; a seam item takes two with kTwoBox.  Over rows of
+  // channels 4 T chunks ran faster than 3; in the API layout 3 + 6 and 4 + 4
+  // ran alike.
+  static constexpr int kTStages = kTwoBox ? 3 : 4;
+  static constexpr int kGStages = kTwoBox ? 6 : 4;
   // a G producer waits on the G stage of its own earlier box: every G stage
   // must stay with one producer, or it would wait on a phase of another's box
   static_assert(kGStages % kGProducers == 0, "a G stage stays with one G producer");
