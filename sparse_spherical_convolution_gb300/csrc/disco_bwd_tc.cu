@@ -48,21 +48,26 @@
 // in rows of channels, where rows are cheap, it arrives as 8 wrapped 8-column
 // boxes in the unswizzled layout, read with that layout's descriptor.
 //
+// Only the input rows of the group with support at the entry's output row
+// take part: the MMAs have N = 32 x those rows and the builders build only
+// their T rows; TMEM starts each tile at zero (the epilogue clears it after
+// reading it out), so every MMA accumulates.
+//
 // Persistent kernel: one CTA per SM; tiles come from the launch's scheduler
 // counter (disco_sched.cuh), in an order that puts the long polar row groups
 // first and keeps the groups that share G rows close; the pipeline runs
-// across tile boundaries.  Rings of 4 G boxes, 4 T chunks and 4 psi blocks;
-// roles:
+// across tile boundaries.  Rings of G boxes (6 in the API layout, 4 over rows
+// of channels), T chunks (3, 4) and 4 psi blocks; roles:
 //   warp 0      tiles: the tile index and the group's entry list (bulk copy)
 //               into one of two info slots; per item the psi block of its
 //               chunk (bulk copy), up to 4 items ahead of the builders;
 //   warp 1      MMA issuer (one thread; descriptors precomputed per stage);
 //   warps 2, 3, 4, 6, 7, 12  build T into the item's stage;
 //   warps 8-11  epilogue: tcgen05.ld, bf16, TMA stores (warp w reads TMEM
-//               lanes 32 (w % 4) ..);
-//   warps 5, 13 G producers: the box of items i % 2 == 0, 1 (the boxes of G
-//               in rows of channels, rows W_out apart, go faster the more
-//               threads issue them).
+//               lanes 32 (w % 4) ..), then zeros back into TMEM;
+//   warps 5, 13 G producers: boxes n % 2 == 0, 1, n counting the boxes (the
+//               boxes of G in rows of channels, rows W_out apart, go faster
+//               the more threads issue them).
 // Warps w and w + 4 share one of the SM's four schedulers: the single-thread
 // MMA issuer and G producers (w % 4 == 1) share theirs with no builder warp.
 // Barriers complete with one arrival per warp (or one commit), not per thread.
